@@ -1,0 +1,175 @@
+/*
+ * lq.h -- C ABI of liblq: per-window int8 recurrent-state decode for Gated
+ * DeltaNet (GDN) and Kimi Delta Attention (KDA) layers on GB300 (sm_103a).
+ *
+ * The method: LeapQuant (paperlayer.ai summary of arXiv 2609.38166v1). Each
+ * head-state S (d_v x d_k = 128 x 128; row i = value channel, column j = key
+ * channel) is held as
+ *   - int8 codes with one fp32 step per value row (sigma),
+ *   - one fp32 smoothing scale per key channel (lambda; §3.4 Residual smoothing),
+ *   - C fp32 Compensator Tokens, each one whole row or column of the state
+ *     (§3.3 Compensator Tokens),
+ * fixed for a window of W tokens (§3.2 Per-window quantization), plus a buffer
+ * of up to W fp32 records (k_m, u_m, alpha_m), one per token of the open window.
+ * Per token, the append step reads the state from the fixed boundary plus the
+ * records (App. B.2 window unrolling, App. B.3 readout with a smoothed
+ * quantized residual), forms the delta-rule correction u, stores the record and
+ * writes the output. When the window is full, the fold rebuilds the state in
+ * original coordinates, selects compensators, smooths, rounds once to int8 and
+ * empties the buffer (fastpathlabs.ai research note 4, "What we built": an
+ * append step and a fold).
+ *
+ * Conventions for every call below:
+ *   - Ownership: the caller owns every buffer. The library allocates no memory
+ *     and creates no streams or events.
+ *   - Pointers: device pointers on the current CUDA device (device or managed
+ *     memory). Token inputs and outputs are contiguous fp32 arrays, 16-byte
+ *     aligned; the state buffer is 256-byte aligned.
+ *   - Layout of token inputs: [n_states][d] row-major, state index
+ *     s = (request * layers + layer) * heads + head, or any order the caller
+ *     keeps fixed.
+ *   - Asynchrony: calls enqueue kernels on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and return without synchronizing. The return
+ *     value covers host-side validation and the launch. Conditions found on
+ *     the device (a full window, a phase mismatch, a state buffer written with
+ *     another configuration) set the state buffer's status word, which
+ *     lq_get_status reads; the affected head-states are left unchanged.
+ *   - Threads: no global mutable state except a thread-local error message.
+ *   - n_states = 0 is valid and does nothing.
+ */
+#ifndef LQ_H
+#define LQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed as an opaque pointer so that this header needs no CUDA headers. */
+typedef void* lq_stream_t;
+
+typedef enum {
+  LQ_OK = 0,
+  LQ_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, pointer not on the current device */
+  LQ_ERR_UNSUPPORTED = -2, /* a configuration this build does not run (see lq_config)            */
+  LQ_ERR_WINDOW_FULL = -3, /* device: append on a head-state that already holds W records         */
+  LQ_ERR_CUDA = -4,        /* a CUDA runtime call failed (message in lq_last_error)              */
+  LQ_ERR_TIMEOUT = -5,     /* device: a bounded wait inside a kernel gave up                       */
+  LQ_ERR_PHASE = -6,       /* device: a head-state's record count differs from the stated phase    */
+  LQ_ERR_STATE = -7        /* device: the state buffer was not initialised with this config/size  */
+} lq_status;
+
+/* lq_decode_step's `phase` when head-states may sit at different window positions. */
+#define LQ_PHASE_ANY (-1)
+
+typedef struct {
+  int32_t d_k, d_v;      /* key / value channels: 128 and 128 in this build                 */
+  int32_t window;        /* W: tokens per window, 1..32 (default 16)                        */
+  int32_t n_comp;        /* C: compensators per head-state, 0..8 (default 4)                */
+  int32_t decay_per_key; /* 0: scalar alpha per token (GDN); 1: alpha in R^{d_k} (KDA)      */
+  int32_t smooth;        /* 1: residual smoothing on (default); 0: lambda = 1               */
+  float lambda_floor;    /* positive floor of the smoothing scales (default 1e-6)           */
+} lq_config;
+
+/*
+ * Byte offsets of the planes inside one state buffer (all 256-byte aligned)
+ * and the per-head-state stride of each plane, in elements. The buffer holds,
+ * for head-state s:
+ *   counts   int32   [s]                       records held (0..W)
+ *   codes    int8    [s][d_v][d_k]             row-major
+ *   sigma    fp32    [s][d_v]                  quantization step of each value row
+ *   lambda   fp32    [s][d_k]                  smoothing scale of each key channel
+ *   comp_id  int32   [s][comp_id_stride]       id < d_v: row id; else column id - d_v
+ *   comp_line fp32   [s][C][128]               the compensator line
+ *   rec_k    fp32    [s][W][d_k]               record keys, slot m-1 holds record m
+ *   rec_u    fp32    [s][W][d_v]               record corrections u_m
+ *   rec_alpha fp32   [s][alpha_stride]         GDN: W scalars; KDA: [W][d_k]
+ * A 256-byte header at offset 0 carries a magic number, a hash of the config
+ * and n_states, and the device status word.
+ * The boundary (codes, sigma, lambda, comp_id, comp_line) takes
+ * (16384 + 512 + 512 + 4C + 512C) bytes per head-state: 1.19 bytes per element
+ * at C = 4, the figure of the LeapQuant summary, §4.3 Efficiency results.
+ */
+typedef struct {
+  size_t total_bytes;
+  size_t header, counts, codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha;
+  int64_t comp_id_stride; /* int32 elements per head-state (C rounded up to a multiple of 4, at least 4) */
+  int64_t alpha_stride;   /* fp32 elements per head-state in rec_alpha                               */
+  int64_t boundary_bytes_per_state; /* codes + sigma + lambda + 4C id bytes + comp lines                  */
+} lq_layout_t;
+
+/* Default configuration: d_k = d_v = 128, W = 16, C = 4, GDN, smoothing on, floor 1e-6. */
+void lq_config_default(lq_config* cfg);
+
+/* Bytes the caller must allocate for n_states head-states (0 if cfg or n_states is invalid). */
+size_t lq_state_bytes(const lq_config* cfg, int64_t n_states);
+
+/* Fill *out with the plane offsets for n_states head-states. Host only; never touches a GPU. */
+int lq_layout(const lq_config* cfg, int64_t n_states, lq_layout_t* out);
+
+/*
+ * Initialise a state buffer: write the header, set every record count to 0 and
+ * init-fold S0 into the boundary (compensator selection, smoothing, rounding;
+ * the fold of §3.3-3.4 without records). S0 is fp32 [n_states][d_v][d_k], or
+ * NULL for the zero state. Clears the status word.
+ */
+int lq_state_init(const lq_config* cfg, void* state, int64_t n_states, const float* S0, lq_stream_t stream);
+
+/*
+ * Append one token to every head-state: read from the fixed boundary plus the
+ * buffered records, u = beta (v - S_{n-1}(alpha . k)), store record n,
+ * o = S_n q. No fold: a head-state that already holds W records is left
+ * unchanged and the status word is set to LQ_ERR_WINDOW_FULL.
+ *   q, k  fp32 [n_states][d_k];  v, o  fp32 [n_states][d_v]
+ *   alpha fp32 [n_states] (GDN) or [n_states][d_k] (KDA);  beta fp32 [n_states]
+ * o may not alias any input.
+ */
+int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k, const float* v,
+              const float* alpha, const float* beta, float* o, lq_stream_t stream);
+
+/* Fold every head-state with the records it holds (any count 0..W), then empty the buffer. */
+int lq_fold(const lq_config* cfg, void* state, int64_t n_states, lq_stream_t stream);
+
+/*
+ * One decode token for every head-state: append, and when that fills the
+ * window (count == W), fold in the same kernel while the state is on chip.
+ * `phase` is the record count every head-state holds before this call
+ * (0..W-1), which lets the library launch the append-only kernel for the W-1
+ * steps that cannot fold; a head-state whose count differs is left unchanged
+ * and sets LQ_ERR_PHASE. LQ_PHASE_ANY accepts any count (each head-state
+ * folds when its own window fills). Arguments otherwise as lq_append.
+ */
+int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
+                   const float* k, const float* v, const float* alpha, const float* beta, float* o,
+                   lq_stream_t stream);
+
+/*
+ * Write the state each head-state stands for, S_n = boundary x Diag(A_n) plus
+ * the buffered records, in original coordinates (the fold's reconstruction,
+ * without rounding), to S_out fp32 [n_states][d_v][d_k]. The state is unchanged.
+ */
+int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, float* S_out, lq_stream_t stream);
+
+/*
+ * Synchronize `stream`, then read the state buffer's status word: LQ_OK or the
+ * first device-side error recorded since lq_state_init / lq_clear_status.
+ * *bad_state (if non-NULL) receives the index of the head-state that set it.
+ */
+int lq_get_status(const void* state, int64_t* bad_state, lq_stream_t stream);
+
+/* Reset the status word to LQ_OK (enqueued on `stream`). */
+int lq_clear_status(void* state, lq_stream_t stream);
+
+/* Thread-local description of the last host-side error of this thread ("" if none). */
+const char* lq_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int lq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LQ_H */

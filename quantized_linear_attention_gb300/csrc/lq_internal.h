@@ -1,0 +1,65 @@
+// Internal declarations shared by the host API (lq_api.cu) and the kernels (lq_kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lq.h"
+
+namespace lqi {
+
+constexpr uint32_t kMagic = 0x4C513847u;  // "GQ8L"
+constexpr uint32_t kLayoutVersion = 1;
+constexpr int kD = 128;       // d_k = d_v
+constexpr int kMaxW = 32;     // records per window
+constexpr int kMaxC = 8;      // compensators per head-state
+constexpr int kThreads = 256; // threads per CTA; one CTA per head-state
+
+// Device-resident header at offset 0 of every state buffer (256 bytes).
+struct Header {
+  uint32_t magic;
+  uint32_t version;
+  uint64_t cfg_hash;
+  int64_t n_states;
+  int32_t status;     // first device-side error (lq_status), 0 when clean
+  int32_t reserved0;
+  int64_t bad_state;  // head-state index that set `status`
+  uint8_t pad[256 - 40];
+};
+static_assert(sizeof(Header) == 256, "header is 256 bytes");
+
+// Everything a kernel needs, passed by value.
+struct Params {
+  int W, C, kda, smooth;
+  float lambda_floor;
+  int phase;  // expected record count before the call, or -1
+  int64_t n_states;
+  uint64_t cfg_hash;
+  int64_t comp_id_stride, alpha_stride;
+  Header* hdr;
+  int32_t* counts;
+  int8_t* codes;
+  float* sigma;
+  float* lambda;
+  int32_t* comp_id;
+  float* comp_line;
+  float* rec_k;
+  float* rec_u;
+  float* rec_alpha;
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* alpha;
+  const float* beta;
+  float* o;
+  const float* S0;  // init source (NULL: zero)
+  float* S_out;     // export target
+};
+
+cudaError_t launch_init(const Params& p, cudaStream_t st);
+cudaError_t launch_append(const Params& p, cudaStream_t st);
+cudaError_t launch_step(const Params& p, cudaStream_t st);
+cudaError_t launch_fold(const Params& p, cudaStream_t st);
+cudaError_t launch_export(const Params& p, cudaStream_t st);
+
+}  // namespace lqi

@@ -1,0 +1,226 @@
+"""Thin Python binding of ``liblq.so`` (C ABI in ``include/lq.h``).
+
+Argument marshalling only: every step of the decode path runs in the library's
+CUDA kernels. Tensors are torch CUDA tensors (PyTorch supplies device memory
+and streams); each call passes their device pointers and the current (or
+given) CUDA stream. The library is loaded on first use; if it is missing the
+call raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+PHASE_ANY = -1
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WINDOW_FULL = -3
+ERR_CUDA = -4
+ERR_TIMEOUT = -5
+ERR_PHASE = -6
+ERR_STATE = -7
+
+STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", -3: "LQ_ERR_WINDOW_FULL",
+                -4: "LQ_ERR_CUDA", -5: "LQ_ERR_TIMEOUT", -6: "LQ_ERR_PHASE", -7: "LQ_ERR_STATE"}
+
+# Every symbol include/lq.h declares.
+EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_append", "lq_fold",
+           "lq_decode_step", "lq_export_state", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("n_comp", ctypes.c_int32), ("decay_per_key", ctypes.c_int32), ("smooth", ctypes.c_int32),
+                ("lambda_floor", ctypes.c_float)]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("total_bytes", "header", "counts", "codes", "sigma", "lambda_",
+                                                "comp_id", "comp_line", "rec_k", "rec_u", "rec_alpha")] + \
+               [("comp_id_stride", ctypes.c_int64), ("alpha_stride", ctypes.c_int64),
+                ("boundary_bytes_per_state", ctypes.c_int64)]
+
+
+class LQError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.lq_library_path()
+
+
+def load():
+    """Load liblq.so (built in-tree by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"liblq.so not found at {path}: build it first (python -c 'import __graft_entry__ as g; "
+                           f"g.build()'); there is no fallback path")
+    L = ctypes.CDLL(path)
+    P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    cfgp = ctypes.POINTER(Config)
+    sig = {
+        "lq_config_default": (None, [cfgp]),
+        "lq_state_bytes": (ctypes.c_size_t, [cfgp, i64]),
+        "lq_layout": (ctypes.c_int, [cfgp, i64, ctypes.POINTER(Layout)]),
+        "lq_state_init": (ctypes.c_int, [cfgp, P, i64, P, P]),
+        "lq_append": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
+        "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
+        "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
+        "lq_export_state": (ctypes.c_int, [cfgp, P, i64, P, P]),
+        "lq_get_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), P]),
+        "lq_clear_status": (ctypes.c_int, [P, P]),
+        "lq_last_error": (ctypes.c_char_p, []),
+        "lq_version": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load().lq_last_error().decode()
+
+
+def _check(rc):
+    if rc != OK:
+        raise LQError(rc, last_error())
+
+
+def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128) -> Config:
+    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor)
+
+
+def default_config() -> Config:
+    c = Config()
+    load().lq_config_default(ctypes.byref(c))
+    return c
+
+
+def state_bytes(cfg: Config, n_states: int) -> int:
+    return int(load().lq_state_bytes(ctypes.byref(cfg), n_states))
+
+
+def layout(cfg: Config, n_states: int) -> Layout:
+    out = Layout()
+    _check(load().lq_layout(ctypes.byref(cfg), n_states, ctypes.byref(out)))
+    return out
+
+
+# ---------------------------------------------------------------------------- marshalling
+def _ptr(t, name, dtype=None):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    import torch
+
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _f32():
+    import torch
+
+    return torch.float32
+
+
+def alloc_state(cfg: Config, n_states: int, device="cuda"):
+    """Caller-owned state buffer (torch supplies the memory)."""
+    import torch
+
+    return torch.empty(state_bytes(cfg, n_states), dtype=torch.uint8, device=device)
+
+
+def state_init(cfg, state, n_states, S0=None, stream=None):
+    _check(load().lq_state_init(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(S0, "S0", _f32()),
+                                _stream(stream)))
+
+
+def append(cfg, state, n_states, q, k, v, alpha, beta, o, stream=None):
+    f = _f32()
+    _check(load().lq_append(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(q, "q", f), _ptr(k, "k", f),
+                            _ptr(v, "v", f), _ptr(alpha, "alpha", f), _ptr(beta, "beta", f), _ptr(o, "o", f),
+                            _stream(stream)))
+
+
+def fold(cfg, state, n_states, stream=None):
+    _check(load().lq_fold(ctypes.byref(cfg), _ptr(state, "state"), n_states, _stream(stream)))
+
+
+def decode_step(cfg, state, n_states, q, k, v, alpha, beta, o, phase=PHASE_ANY, stream=None):
+    f = _f32()
+    _check(load().lq_decode_step(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(phase), _ptr(q, "q", f),
+                                 _ptr(k, "k", f), _ptr(v, "v", f), _ptr(alpha, "alpha", f), _ptr(beta, "beta", f),
+                                 _ptr(o, "o", f), _stream(stream)))
+
+
+def export_state(cfg, state, n_states, S_out, stream=None):
+    _check(load().lq_export_state(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(S_out, "S_out", _f32()),
+                                  _stream(stream)))
+
+
+def get_status(state, stream=None):
+    """(status, bad_state): synchronizes the stream and reads the device status word."""
+    bad = ctypes.c_int64(-1)
+    rc = load().lq_get_status(_ptr(state, "state"), ctypes.byref(bad), _stream(stream))
+    if rc in (ERR_INVALID_ARG, ERR_CUDA):
+        raise LQError(rc, last_error())
+    return rc, bad.value
+
+
+def clear_status(state, stream=None):
+    _check(load().lq_clear_status(_ptr(state, "state"), _stream(stream)))
+
+
+def state_views(cfg: Config, state, n_states: int) -> dict:
+    """Typed torch views of the planes of a state buffer (no copy), per ``lq_layout``."""
+    import torch
+
+    L = layout(cfg, n_states)
+    N, D, W, C = n_states, cfg.d_k, cfg.window, cfg.n_comp
+
+    def view(off, count, dtype, shape):
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return state[off:off + nbytes].view(dtype).view(*shape)
+
+    return {
+        "counts": view(L.counts, N, torch.int32, (N,)),
+        "codes": view(L.codes, N * D * D, torch.int8, (N, D, D)),
+        "sigma": view(L.sigma, N * D, torch.float32, (N, D)),
+        "lambda": view(L.lambda_, N * D, torch.float32, (N, D)),
+        "comp_id": view(L.comp_id, N * L.comp_id_stride, torch.int32, (N, L.comp_id_stride))[:, :C],
+        "comp_line": view(L.comp_line, N * C * D, torch.float32, (N, C, D)),
+        "rec_k": view(L.rec_k, N * W * D, torch.float32, (N, W, D)),
+        "rec_u": view(L.rec_u, N * W * D, torch.float32, (N, W, D)),
+        "rec_alpha": view(L.rec_alpha, N * L.alpha_stride, torch.float32, (N, L.alpha_stride)),
+    }

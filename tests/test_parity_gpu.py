@@ -1,0 +1,67 @@
+"""GPU vs oracle parity through the C ABI (free-running, element by element).
+
+Outputs o within 1e-4 relative L2 per (head-state, token); int8 codes and
+compensator ids bit-exact except codes within 1e-6 relative of a rounding tie
+(fewer than 1e-5 of entries, at most one code apart); sigma, lambda, compensator
+lines, record u and the exported state bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from quantized_linear_attention_gb300 import lq
+from quantized_linear_attention_gb300 import workload as wlm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lq.load()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("phase_mode", ["stated", "any"])
+def test_tiny_gdn_workload_full(phase_mode):
+    from tests._gpu import run_and_compare
+
+    wl = wlm.WORKLOADS[1]
+    run_and_compare(wl, wl.n_tokens, phase_mode=phase_mode)
+
+
+@pytest.mark.parametrize("n", [1, 3, 33, 157, 305])
+def test_ragged_batches_warm_planted(n):
+    from tests._gpu import run_and_compare
+
+    wl = wlm.custom(200 + n, n, 0, n_warm=48, plant=True)
+    run_and_compare(wl, 2 * 16 + 5)
+
+
+def test_kda_t3_small():
+    from tests._gpu import run_and_compare
+
+    wl = wlm.WORKLOADS[5]
+    small = wlm.Workload(wl.wid, wl.name, 6, 40, True, "t3", 512, False, 1, 1, 6)
+    run_and_compare(small, small.n_tokens)
+
+
+@pytest.mark.parametrize("W,C,smooth", [(1, 0, False), (7, 3, True), (32, 8, True), (16, 4, False), (5, 0, True)])
+def test_window_and_compensator_variants(W, C, smooth):
+    from tests._gpu import run_and_compare
+
+    wl = wlm.custom(300 + W * 10 + C, 9, 0, n_warm=32, plant=True)
+    run_and_compare(wl, 2 * W + 3, W=W, C=C, smooth=smooth)
+
+
+def test_kda_variants():
+    from tests._gpu import run_and_compare
+
+    wl = wlm.custom(390, 5, 0, kda=True, vdist="t3", n_warm=40)
+    run_and_compare(wl, 2 * 7 + 2, W=7, C=5)
+
+
+def test_separate_append_and_fold_match_fused_step():
+    from tests._gpu import run_and_compare
+
+    wl = wlm.custom(400, 11, 0, n_warm=40, plant=True)
+    run_and_compare(wl, 2 * 16 + 4, use_append_fold=True)
