@@ -63,7 +63,8 @@ def build_workload(force: bool = False) -> str:
         return out
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O3", "-std=c11", "-fPIC", "-shared", "-pthread", src, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", "-O3", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", src, "-o", tmp,
+                    "-lm"], check=True)
     os.replace(tmp, out)
     return out
 

@@ -20,6 +20,7 @@
 // behind the source's back. The output o is compared with a tolerance and its
 // order is free.
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "lq_internal.h"
@@ -145,16 +146,24 @@ namespace lqi {
 // smoothing scales act on the residual term only), §3.3 (compensators are
 // records at window position 0 carrying the full decay A_n).
 
+// Vectors read as float4 come first; every array size is a multiple of 4 floats
+// so each member starts on a 16-byte boundary.
 template <bool KDA>
-struct AppendSmem {
-  float P[(kMaxW + 1) * (KDA ? kD : 1)];  // decay products P_m, m = 0..n
-  float kn[kD], qn[kD];                    // current token's k, q
-  float y[kD], aq[kD];                     // A_n . k_n and A_n . q_n
-  float zk[kD], zq[kD];                    // lambda . y, lambda . (A_n . q_n)
-  float basek[kD], baseq[kD];              // sigma_i * dot(Cd[i,:], z)
-  float g[kMaxW + 1], h[kMaxW + 1];        // record reads: k_m . (P_m . k_n), k_m . (P_m . q_n)
-  float ec[kMaxC], eq[kMaxC];              // compensator reads b_c . y, b_c . (A_n . q_n)
+struct alignas(16) AppendSmem {
+  float kn[kD], qn[kD];                                 // current token's k, q
+  float y[kD], aq[kD];                                  // A_n . k_n and A_n . q_n
+  float zk[kD], zq[kD];                                 // lambda . y, lambda . (A_n . q_n)
+  float basek[kD], baseq[kD];                           // sigma_i * dot(Cd[i,:], z)
+  float P[((kMaxW + 1) * (KDA ? kD : 1) + 3) / 4 * 4];  // decay products P_m, m = 0..n
+  float g[(kMaxW + 1 + 3) / 4 * 4];                     // record reads k_m . (P_m . k_n)
+  float h[(kMaxW + 1 + 3) / 4 * 4];                     // output terms k_m . (P_m . q_n)
+  float ec[kMaxC], eq[kMaxC];                           // compensator reads b_c . y, b_c . (A_n . q_n)
 };
+static_assert(offsetof(AppendSmem<false>, zk) % 16 == 0 && offsetof(AppendSmem<false>, zq) % 16 == 0,
+              "float4 loads of z need 16-byte alignment");
+static_assert(offsetof(AppendSmem<true>, zk) % 16 == 0 && sizeof(AppendSmem<false>) % 16 == 0 &&
+                  sizeof(AppendSmem<true>) % 16 == 0,
+              "dynamic shared memory after AppendSmem stays 16-byte aligned");
 
 template <bool KDA>
 __device__ __forceinline__ void append_body(const Params& p, int64_t s, int n, AppendSmem<KDA>& sm) {

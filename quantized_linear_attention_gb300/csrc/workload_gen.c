@@ -17,7 +17,7 @@
  * Distributions (one linear-attention layer of Qwen3.5-9B: 128x128 state per
  * head, per the fastpathlabs.ai research note, "Background"):
  *   uniform  u = ((x >> 11) + 0.5) * 2^-53, in (0, 1)
- *   normal   Box-Muller, cosine branch, in double
+ *   normal   Box-Muller in double (cosine branch for even, sine for odd counters)
  *   t(3)     z0 / sqrt((z1^2 + z2^2 + z3^2) / 3)
  *   q, k     normal, L2-normalised in double, then rounded to fp32
  *   v        normal (GDN workloads) or Student-t(3) (KDA workload)
@@ -27,9 +27,9 @@
  *
  * Initial state: n_warm tokens of the plain (unquantized) gated delta rule,
  *   S_t = S_{t-1} Diag(alpha_t) + u_t k_t^T,  u_t = beta_t (v_t - S_{t-1}(alpha_t . k_t)),
- * run in double from zero (the model's own recurrence, used here only to give
- * the state realistic structure), then optionally two rows and two columns
- * scaled by 30 to plant outliers, then rounded once to fp32.
+ * run in fp32 from zero (the model's own recurrence, used here only to give the
+ * state realistic structure), then optionally two rows and two columns scaled
+ * by 30 to plant outliers (intersections by 900).
  *
  * Build: plain C11, no CUDA. Threads split the state range.
  */
@@ -76,12 +76,28 @@ static inline double wl_uniform(uint64_t key, uint64_t e) {
   return ((double)(wl_raw(key, e) >> 11) + 0.5) * (1.0 / 9007199254740992.0);
 }
 
-/* Box-Muller, cosine branch: uses raw counters 2e and 2e+1. */
+/* Box-Muller: the pair (2m, 2m+1) of normals comes from uniforms at raw
+ * counters 2m and 2m+1; even e takes the cosine branch, odd e the sine branch. */
 static inline double wl_normal(uint64_t key, uint64_t e) {
   const double two_pi = 6.283185307179586476925286766559;
-  double u1 = wl_uniform(key, 2 * e);
-  double u2 = wl_uniform(key, 2 * e + 1);
-  return sqrt(-2.0 * log(u1)) * cos(two_pi * u2);
+  const uint64_t m = e >> 1;
+  double u1 = wl_uniform(key, 2 * m);
+  double u2 = wl_uniform(key, 2 * m + 1);
+  double rad = sqrt(-2.0 * log(u1));
+  return (e & 1) ? rad * sin(two_pi * u2) : rad * cos(two_pi * u2);
+}
+
+/* normals e = 0..d-1 into out, two per Box-Muller draw */
+static void wl_normals(uint64_t key, int d, double* out) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int e = 0; e < d; e += 2) {
+    const uint64_t m = (uint64_t)e >> 1;
+    double u1 = wl_uniform(key, 2 * m);
+    double u2 = wl_uniform(key, 2 * m + 1);
+    double rad = sqrt(-2.0 * log(u1));
+    out[e] = rad * cos(two_pi * u2);
+    if (e + 1 < d) out[e + 1] = rad * sin(two_pi * u2);
+  }
 }
 
 /* Student-t with 3 degrees of freedom: four normals at counters 4e..4e+3. */
@@ -96,10 +112,8 @@ static inline double wl_student_t3(uint64_t key, uint64_t e) {
 static void wl_unit_vector(uint64_t key, int d, float* out) {
   double buf[1024];
   double ss = 0.0;
-  for (int j = 0; j < d; ++j) {
-    buf[j] = wl_normal(key, (uint64_t)j);
-    ss += buf[j] * buf[j];
-  }
+  wl_normals(key, d, buf);
+  for (int j = 0; j < d; ++j) ss += buf[j] * buf[j];
   double inv = 1.0 / sqrt(ss);
   for (int j = 0; j < d; ++j) out[j] = (float)(buf[j] * inv);
 }
@@ -112,6 +126,22 @@ static float wl_alpha_scalar_clipped(uint64_t key) {
   if (a < lo) a = lo;
   if (a > hi) a = hi;
   return a;
+}
+
+static void wl_values(uint64_t key, int vdist, int d, float* out) {
+  double buf[1024];
+  if (vdist) {
+    for (int i = 0; i < d; ++i) out[i] = (float)wl_student_t3(key, (uint64_t)i);
+  } else {
+    wl_normals(key, d, buf);
+    for (int i = 0; i < d; ++i) out[i] = (float)buf[i];
+  }
+}
+
+static void wl_alpha_vector(uint64_t key, int d, float* out) {
+  double buf[1024];
+  wl_normals(key, d, buf);
+  for (int c = 0; c < d; ++c) out[c] = (float)(1.0 / (1.0 + exp(buf[c])));
 }
 
 static float wl_beta(uint64_t key) {
@@ -142,15 +172,12 @@ static void wl_token_states(const wl_job* j) {
       if (j->k) wl_unit_vector(wl_key(j->seed, j->wl, gs, tok, WL_T_K), dk, j->k + row * dk);
       if (j->v) {
         uint64_t kv = wl_key(j->seed, j->wl, gs, tok, WL_T_V);
-        float* vp = j->v + row * dv;
-        for (int i = 0; i < dv; ++i)
-          vp[i] = (float)(j->vdist ? wl_student_t3(kv, (uint64_t)i) : wl_normal(kv, (uint64_t)i));
+        wl_values(kv, j->vdist, dv, j->v + row * dv);
       }
       if (j->alpha) {
         uint64_t ka = wl_key(j->seed, j->wl, gs, tok, WL_T_ALPHA);
         if (j->kda) {
-          float* ap = j->alpha + row * dk;
-          for (int c = 0; c < dk; ++c) ap[c] = (float)(1.0 / (1.0 + exp(wl_normal(ka, (uint64_t)c))));
+          wl_alpha_vector(ka, dk, j->alpha + row * dk);
         } else {
           j->alpha[row] = wl_alpha_scalar_clipped(ka);
         }
@@ -165,65 +192,70 @@ static void* wl_token_thread(void* p) {
   return NULL;
 }
 
-/* Plain delta-rule warm-up in double for one state, then planting. */
+/* Plain delta-rule warm-up in fp32 for one state, then planting. The state is
+ * kept column-major (ST[c][i] = S[i][c]) so that every inner loop runs over the
+ * value rows i: each entry sees the same sequence of roundings in any build. */
 static void wl_initial_one(const wl_job* j, int64_t s) {
   const int dk = j->dk, dv = j->dv;
   const uint64_t gs = (uint64_t)(j->state0 + s);
-  double* S = (double*)calloc((size_t)dv * dk, sizeof(double));
-  double* ak = (double*)malloc(sizeof(double) * dk);
-  double* a = (double*)malloc(sizeof(double) * dk);
+  float* ST = (float*)calloc((size_t)dv * dk, sizeof(float));
+  float* r = (float*)malloc(sizeof(float) * dv);
+  float* u = (float*)malloc(sizeof(float) * dv);
+  float* vf = (float*)malloc(sizeof(float) * dv);
+  float* a = (float*)malloc(sizeof(float) * dk);
   float* kf = (float*)malloc(sizeof(float) * dk);
   for (int t = 0; t < j->n_warm; ++t) {
     const uint64_t tok = (uint64_t)t;
     wl_unit_vector(wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_K), dk, kf);
-    uint64_t ka = wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_ALPHA);
+    const uint64_t ka = wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_ALPHA);
     if (j->kda) {
-      for (int c = 0; c < dk; ++c) a[c] = (double)(float)(1.0 / (1.0 + exp(wl_normal(ka, (uint64_t)c))));
+      wl_alpha_vector(ka, dk, a);
     } else {
-      double as = (double)wl_alpha_scalar_clipped(ka);
+      const float as = wl_alpha_scalar_clipped(ka);
       for (int c = 0; c < dk; ++c) a[c] = as;
     }
-    const double beta = (double)wl_beta(wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_BETA));
-    const uint64_t kv = wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_V);
-    for (int c = 0; c < dk; ++c) ak[c] = a[c] * (double)kf[c];
-    for (int i = 0; i < dv; ++i) {
-      double* Si = S + (size_t)i * dk;
-      double r = 0.0;
-      for (int c = 0; c < dk; ++c) r += Si[c] * ak[c];
-      double vi = (double)(float)(j->vdist ? wl_student_t3(kv, (uint64_t)i) : wl_normal(kv, (uint64_t)i));
-      double u = beta * (vi - r);
-      for (int c = 0; c < dk; ++c) Si[c] = Si[c] * a[c] + u * (double)kf[c];
+    const float beta = wl_beta(wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_BETA));
+    wl_values(wl_key(j->seed, j->wl, gs, tok, WL_T_WARM_V), j->vdist, dv, vf);
+    for (int i = 0; i < dv; ++i) r[i] = 0.0f;
+    for (int c = 0; c < dk; ++c) {
+      const float akc = a[c] * kf[c];
+      const float* col = ST + (size_t)c * dv;
+      for (int i = 0; i < dv; ++i) r[i] = r[i] + col[i] * akc;
+    }
+    for (int i = 0; i < dv; ++i) u[i] = beta * (vf[i] - r[i]);
+    for (int c = 0; c < dk; ++c) {
+      const float ac = a[c], kc = kf[c];
+      float* col = ST + (size_t)c * dv;
+      for (int i = 0; i < dv; ++i) col[i] = col[i] * ac + u[i] * kc;
     }
   }
+  int i1 = -1, i2 = -1, c1 = -1, c2 = -1;
   if (j->plant) {
     uint64_t kp = wl_key(j->seed, j->wl, gs, 0, WL_T_PLANT);
-    int i1 = (int)(wl_uniform(kp, 0) * dv);
-    int i2 = (i1 + 1 + (int)(wl_uniform(kp, 1) * (dv - 1))) % dv;
-    int c1 = (int)(wl_uniform(kp, 2) * dk);
-    int c2 = (c1 + 1 + (int)(wl_uniform(kp, 3) * (dk - 1))) % dk;
-    for (int c = 0; c < dk; ++c) {
-      S[(size_t)i1 * dk + c] *= 30.0;
-      S[(size_t)i2 * dk + c] *= 30.0;
-    }
-    for (int i = 0; i < dv; ++i) {
-      S[(size_t)i * dk + c1] *= 30.0;
-      S[(size_t)i * dk + c2] *= 30.0;
-    }
-    if (j->planted) {
-      int32_t* pl = j->planted + 4 * s;
-      pl[0] = i1;
-      pl[1] = i2;
-      pl[2] = c1;
-      pl[3] = c2;
-    }
-  } else if (j->planted) {
-    int32_t* pl = j->planted + 4 * s;
-    pl[0] = pl[1] = pl[2] = pl[3] = -1;
+    i1 = (int)(wl_uniform(kp, 0) * dv);
+    i2 = (i1 + 1 + (int)(wl_uniform(kp, 1) * (dv - 1))) % dv;
+    c1 = (int)(wl_uniform(kp, 2) * dk);
+    c2 = (c1 + 1 + (int)(wl_uniform(kp, 3) * (dk - 1))) % dk;
   }
   float* out = j->S0 + (size_t)s * dv * dk;
-  for (size_t e = 0; e < (size_t)dv * dk; ++e) out[e] = (float)S[e];
-  free(S);
-  free(ak);
+  for (int i = 0; i < dv; ++i) {
+    const float fi = (i == i1 || i == i2) ? 30.0f : 1.0f;
+    for (int c = 0; c < dk; ++c) {
+      const float fc = (c == c1 || c == c2) ? 30.0f : 1.0f;
+      out[(size_t)i * dk + c] = ST[(size_t)c * dv + i] * fi * fc;
+    }
+  }
+  if (j->planted) {
+    int32_t* pl = j->planted + 4 * s;
+    pl[0] = i1;
+    pl[1] = i2;
+    pl[2] = c1;
+    pl[3] = c2;
+  }
+  free(ST);
+  free(r);
+  free(u);
+  free(vf);
   free(a);
   free(kf);
 }
