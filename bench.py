@@ -1,0 +1,559 @@
+#!/usr/bin/env python
+"""Benchmark: per-window int8 recurrent-state decode for one GDN layer on GB300.
+
+Workload (default): one Gated DeltaNet linear-attention layer shaped like
+Qwen3.5-9B's, batch 512 requests x 32 heads = 16,384 head-states of 128 x 128,
+W = 16, C = 4, seeded synthetic inputs, initial state from 512 warm-up tokens
+with planted outlier lines.
+
+One step = one window of W = 16 decode tokens for every head-state: 15
+append-only launches and one fused append+fold launch of ``lq_decode_step``,
+so every step of the hot path (decay products, fused dequantize+matvec,
+compensator and record terms, the delta-rule correction and the fold) runs once
+per head-state per token. The metric is head-tokens/s (head-states x tokens per
+second) plus the achieved HBM bandwidth of the dominant kernel against the
+measured copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints ONE JSON line. Under torchrun every rank runs the full workload
+on its own GPU (head-states are independent: weak scaling, no collective on
+the data path); the timed region is bracketed by barriers and the time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "head-tokens/s and achieved HBM GB/s (% of GB300 peak) at batch 32/128/512"
+UNIT = "head-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_append_gdn_batch512.md")
+KERNEL_SOURCE = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc", "lq_kernels.cu")
+
+
+# ----------------------------------------------------------------------------- bytes
+def alg_bytes_append(p, C=4, kda=False, D=128):
+    """Algorithmic bytes one head-state moves in an append at window phase p
+    (p records held before the token): every input read once, every output written once."""
+    alen = D if kda else 1
+    rec = 4 * D + 4 * D + 4 * alen  # k, u, alpha of one record
+    reads = D * D + 4 * D + 4 * D + 4 * C + 4 * C * D  # boundary: codes, sigma, lambda, ids, lines
+    reads += p * rec + 4  # buffered records, record count
+    reads += 4 * D * 3 + 4 * alen + 4  # q, k, v, alpha, beta
+    writes = rec + 4 * D + 4  # new record, o, record count
+    return reads + writes
+
+
+def alg_bytes_fold_extra(C=4, D=128):
+    """Bytes the fold adds to the append that fills the window: the new boundary."""
+    return D * D + 4 * D + 4 * D + 4 * C + 4 * C * D
+
+
+def alg_bytes_window(W=16, C=4, kda=False):
+    """Per head-state per window: W-1 appends and one fused append+fold."""
+    return sum(alg_bytes_append(p, C, kda) for p in range(W)) + alg_bytes_fold_extra(C)
+
+
+# ----------------------------------------------------------------------------- environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def profile_traffic():
+    """(bytes per launch, note) from the committed ncu summary of the dominant kernel,
+    or (None, why) when there is none or the kernel source changed since it was taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None, "no ncu summary committed"
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    if fields.get("kernel_source_sha256") != src:
+        return None, "kernel changed since the ncu capture"
+    try:
+        return float(fields["dram_bytes_per_launch"]), "ncu capture"
+    except (KeyError, ValueError):
+        return None, "summary lacks dram_bytes_per_launch"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0, period_ms=50):
+        self.tmp = tempfile.NamedTemporaryFile(prefix="lq_clocks_", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.close()
+        try:
+            text = open(self.tmp.name).read()
+        finally:
+            os.unlink(self.tmp.name)
+        return self.summarize(text, self.t0, self.t1)
+
+    @staticmethod
+    def summarize(text, t0=None, t1=None):
+        rows = []
+        for rec in csv.reader(io.StringIO(text)):
+            if len(rec) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(rec[2]), float(rec[3]), [x.strip() for x in rec[5:]]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 is not None and t0 - 1 <= r[0] <= (t1 or r[0]) + 1]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def workload_config(wl, pool_tokens):
+    return {"workload": wl.name, "n_states": wl.n_states, "batch": wl.requests, "layers": wl.layers,
+            "heads": wl.heads, "d_k": wl.dk, "d_v": wl.dv, "W": wl.W, "C": wl.C,
+            "decay": "per-key (KDA)" if wl.kda else "scalar (GDN)", "tokens_per_step": wl.W,
+            "state_storage": "int8 codes + fp32 scales, compensators, records",
+            "l2": f"inputs larger than L2: the state buffer and a {pool_tokens}-token input pool exceed 129 MB; "
+                  f"no flush"}
+
+
+class Pool:
+    """A pool of token inputs resident in HBM (or pinned on the host for the end-to-end leg)."""
+
+    def __init__(self, wl, n_tokens, device, pinned=False, on_device=True):
+        import numpy as np
+        import torch
+
+        from quantized_linear_attention_gb300 import workload as wlm
+
+        tk = wlm.tokens(wl, 0, n_tokens)
+        self.n_tokens = n_tokens
+        self.host = [torch.from_numpy(np.ascontiguousarray(x)) for x in (tk.q, tk.k, tk.v, tk.alpha, tk.beta)]
+        if pinned:
+            self.host = [h.pin_memory() for h in self.host]
+        self.dev = [h.to(device) for h in self.host] if on_device else None
+
+    def token(self, t):
+        t %= self.n_tokens
+        return [x[t] for x in self.dev]
+
+
+def setup_state(wl, device):
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    cfg = lq.config(window=wl.W, n_comp=wl.C, kda=wl.kda)
+    S0, _ = wlm.initial_state(wl)
+    state = lq.alloc_state(cfg, wl.n_states, device)
+    lq.state_init(cfg, state, wl.n_states, None if S0 is None else torch.from_numpy(S0).to(device))
+    del S0
+    return cfg, state
+
+
+def time_main(wl, args, device, world):
+    """The timed region: K windows, a CUDA event between every two launches."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+
+    W, N = wl.W, wl.n_states
+    cfg, state = setup_state(wl, device)
+    pool = Pool(wl, 4 * W, device)
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+
+    def launch(t):
+        q, k, v, a, b = pool.token(t)
+        lq.decode_step(cfg, state, N, q, k, v, a, b, o, phase=t % W)
+
+    tok = 0
+    for _ in range(args.warmup):
+        for _ in range(W):
+            launch(tok)
+            tok += 1
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K * W + 1)]
+    sampler = ClockSampler(device.index or 0)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    ev[0].record()
+    for i in range(K * W):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    barrier(world)
+    clocks = sampler.stop()
+    status, bad = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
+    if not torch.isfinite(o).all():
+        raise RuntimeError("non-finite output")
+    total_ms = ev[0].elapsed_time(ev[-1])
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(K * W)]
+    app = [d[i] for i in range(K * W) if i % W != W - 1]
+    fold = [d[i] for i in range(K * W) if i % W == W - 1]
+    del state, pool
+    torch.cuda.empty_cache()
+    return total_ms, app, fold, clocks
+
+
+def time_graphed(wl, steps, device):
+    """Small batches are launch-bound: capture the W-1 appends and the fold step as
+    two CUDA graphs per pool window and time their replays."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+
+    W, N = wl.W, wl.n_states
+    cfg, state = setup_state(wl, device)
+    n_pool_windows = 4
+    pool = Pool(wl, n_pool_windows * W, device)
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+    graphs = []
+    side = torch.cuda.Stream(device)
+    for wi in range(n_pool_windows):
+        ga, gf = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=side, capture_error_mode="relaxed"):
+            for p in range(W - 1):
+                q, k, v, a, b = pool.token(wi * W + p)
+                lq.decode_step(cfg, state, N, q, k, v, a, b, o, phase=p)
+        with torch.cuda.graph(gf, stream=side, capture_error_mode="relaxed"):
+            q, k, v, a, b = pool.token(wi * W + W - 1)
+            lq.decode_step(cfg, state, N, q, k, v, a, b, o, phase=W - 1)
+        graphs.append((ga, gf))
+    for i in range(3):
+        ga, gf = graphs[i % n_pool_windows]
+        ga.replay()
+        gf.replay()
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+    e[0].record()
+    for i in range(steps):
+        ga, gf = graphs[i % n_pool_windows]
+        ga.replay()
+        e[2 * i + 1].record()
+        gf.replay()
+        e[2 * i + 2].record()
+    torch.cuda.synchronize()
+    status, _ = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)}")
+    total = e[0].elapsed_time(e[-1])
+    app = statistics.median(e[2 * i].elapsed_time(e[2 * i + 1]) for i in range(steps)) / (W - 1)
+    fold = statistics.median(e[2 * i + 1].elapsed_time(e[2 * i + 2]) for i in range(steps))
+    del graphs, state, pool
+    torch.cuda.empty_cache()
+    return total, app, fold
+
+
+def time_e2e(wl, steps, device):
+    """End to end through the C ABI with host buffers: each step copies that
+    window's inputs from pinned host memory, runs the 16 decode calls and copies
+    the 16 outputs back, all inside the timed region."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+
+    W, N = wl.W, wl.n_states
+    cfg, state = setup_state(wl, device)
+    n_pool_windows = 2
+    pool = Pool(wl, n_pool_windows * W, device, pinned=True, on_device=False)
+    stage = [torch.empty((W,) + tuple(h.shape[1:]), dtype=h.dtype, device=device) for h in pool.host]
+    o_dev = torch.empty((W, N, wl.dv), dtype=torch.float32, device=device)
+    o_host = torch.empty((W, N, wl.dv), dtype=torch.float32).pin_memory()
+    h2d = sum(s.numel() * s.element_size() for s in stage)
+    d2h = o_host.numel() * o_host.element_size()
+
+    def step(i):
+        wi = i % n_pool_windows
+        for s, h in zip(stage, pool.host):
+            s.copy_(h[wi * W:(wi + 1) * W], non_blocking=True)
+        for p in range(W):
+            lq.decode_step(cfg, state, N, stage[0][p], stage[1][p], stage[2][p], stage[3][p], stage[4][p],
+                           o_dev[p], phase=p)
+        o_host.copy_(o_dev, non_blocking=True)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    status, _ = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)}")
+    del state, stage, o_dev
+    torch.cuda.empty_cache()
+    return ms, h2d, d2h
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle as it stands, on all host cores, over a bounded sample: M
+    head-states x one window (16 tokens, fold included)."""
+    import oracle
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    cores = os.cpu_count() or 1
+    W = wl.W
+
+    def run(M):
+        S0, _ = wlm.initial_state(wl, 0, M)
+        tk = wlm.tokens(wl, 0, W, 0, M)
+        st = oracle.OracleState(M, W=W, C=wl.C, decay_per_key=wl.kda)
+        st.init(S0)
+        t0 = time.perf_counter()
+        st.run(tk.q, tk.k, tk.v, tk.alpha, tk.beta, nthreads=cores, want_o=True)
+        return time.perf_counter() - t0
+
+    m0 = min(wl.n_states, max(cores, 32))
+    rate = m0 * W / run(m0)
+    M = int(min(wl.n_states, max(m0, rate * budget_s / W)))
+    dt = run(M)
+    return {"value": round(M * W / dt, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{M} of {wl.n_states} head-states x {W} tokens (one window, fold included) of {wl.name}; "
+                      f"{dt:.1f} s on {cores} threads ({os.uname().machine})"}
+
+
+def run_ours(args):
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    lq.load()
+    wl = wlm.WORKLOADS[args.workload]
+    W, N, K = wl.W, wl.n_states, args.steps
+    total_ms, app, fold, clocks = time_main(wl, args, device, world)
+    t_ms = max_over_ranks(total_ms, world, device)
+    value = world * N * W * K / (t_ms / 1e3)
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    app_bytes = N * statistics.mean(alg_bytes_append(p, wl.C, wl.kda) for p in range(W - 1))
+    app_ms = statistics.mean(app)
+    fold_ms = statistics.mean(fold)
+    achieved = app_bytes / (app_ms / 1e3) / 1e9
+    traffic, traffic_note = profile_traffic()
+    fold_bytes = N * (alg_bytes_append(W - 1, wl.C, wl.kda) + alg_bytes_fold_extra(wl.C))
+    win_bytes = N * alg_bytes_window(W, wl.C, wl.kda)
+    win_gbs = win_bytes / (t_ms / K / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(wl, 4 * W), parallelism=f"replicas x{world} (independent head-states)"),
+        "roofline": {"bound": "hbm", "kernel": "k_append (append-only decode step, phases 0..14)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "alg_bytes_per_launch": round(app_bytes), "launch_ms": round(app_ms, 5)},
+        "fold_step": {"kernel": "k_step (append + fold, phase 15)", "launch_ms": round(fold_ms, 5),
+                      "alg_bytes_per_launch": round(fold_bytes),
+                      "achieved_gbs": round(fold_bytes / (fold_ms / 1e3) / 1e9, 1),
+                      "fold_cost_per_token_ms": round((fold_ms - app_ms) / W, 5),
+                      "amortized_below_one_append": (fold_ms - app_ms) / W < app_ms},
+        "window": {"alg_bytes": win_bytes, "achieved_gbs": round(win_gbs, 1), "frac": round(win_gbs / hbm, 4),
+                   "alg_bytes_per_head_token": round(win_bytes / N / W, 1)},
+        "gpu_launches": K * W,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_sweep:
+        sweep = {}
+        for wid in (2, 3):
+            swl = wlm.WORKLOADS[wid]
+            total, a_ms, f_ms = time_graphed(swl, args.sweep_steps, device)
+            wb = swl.n_states * alg_bytes_window(swl.W, swl.C, swl.kda)
+            gbs = wb / (total / args.sweep_steps / 1e3) / 1e9
+            sweep[f"batch{swl.requests}"] = {
+                "head_tokens_per_s": round(swl.n_states * swl.W * args.sweep_steps / (total / 1e3), 1),
+                "append_step_us": round(a_ms * 1e3, 2), "fold_step_us": round(f_ms * 1e3, 2),
+                "window_gbs": round(gbs, 1), "window_frac": round(gbs / hbm, 4),
+                "note": "CUDA-graph replays; the working set may sit in L2 (effective bandwidth)"}
+        sweep[f"batch{wl.requests}"] = {
+            "head_tokens_per_s": round(value / world, 1), "append_step_us": round(app_ms * 1e3, 2),
+            "fold_step_us": round(fold_ms * 1e3, 2), "window_gbs": round(win_gbs, 1),
+            "window_frac": round(win_gbs / hbm, 4)}
+        result["batches"] = sweep
+    if rank == 0 and args.e2e_steps > 0:
+        ms, h2d, d2h = time_e2e(wl, args.e2e_steps, device)
+        result["e2e"] = {"value": round(N * W * args.e2e_steps / (ms / 1e3), 1), "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "note": "pinned host inputs -> device, 16 lq_decode_step calls, outputs -> host"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle as the reference arm, on this machine's host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    wl = wlm.WORKLOADS[args.workload]
+    W = wl.W
+    cores = os.cpu_count() or 1
+    budget = float(os.environ.get("LQ_REFERENCE_BUDGET_S", "120"))
+    m0 = min(wl.n_states, max(cores, 16))
+    S0, _ = wlm.initial_state(wl, 0, m0)
+    tk = wlm.tokens(wl, 0, W, 0, m0)
+    st = oracle.OracleState(m0, W=W, C=wl.C, decay_per_key=wl.kda)
+    st.init(S0)
+    t0 = time.perf_counter()
+    st.run(tk.q, tk.k, tk.v, tk.alpha, tk.beta, nthreads=cores)
+    rate = m0 * W / (time.perf_counter() - t0)
+    per_step_s = budget / max(args.steps + args.warmup, 1)
+    M = int(min(wl.n_states, max(cores, rate * per_step_s / W)))
+    S0, _ = wlm.initial_state(wl, 0, M)
+    pool = wlm.tokens(wl, 0, 2 * W, 0, M)
+    st = oracle.OracleState(M, W=W, C=wl.C, decay_per_key=wl.kda)
+    st.init(S0)
+
+    def step(i):
+        sl = slice((i % 2) * W, (i % 2 + 1) * W)
+        st.run(pool.q[sl], pool.k[sl], pool.v[sl], pool.alpha[sl], pool.beta[sl], nthreads=cores)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = M * W * args.steps / dt
+    sample = f"{M} of {wl.n_states} head-states x {W} tokens per step (one window, fold included) of {wl.name}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(wl, 2 * W), parallelism="host cores (oracle)"),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400, help="timed windows (16 decode tokens each)")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up windows")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=4, help="workload id (4 = batch 512)")
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
