@@ -119,8 +119,14 @@ int current_device(int* dev) {
 
 int check_stream(lq_stream_t stream, int dev) {
   if (!stream) return LQ_OK;
+  // A stream being captured into a CUDA graph may not be queried for its
+  // device; its kernels are checked when the graph is instantiated.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone) return LQ_OK;
   int sdev = -1;
-  cudaError_t e = cudaStreamGetDevice((cudaStream_t)stream, &sdev);
+  e = cudaStreamGetDevice((cudaStream_t)stream, &sdev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetDevice");
   if (sdev != dev) return fail(LQ_ERR_INVALID_ARG, "stream belongs to device %d, current device is %d", sdev, dev);
   return LQ_OK;
