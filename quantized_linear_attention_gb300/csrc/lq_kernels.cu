@@ -5,8 +5,17 @@
 // unrolling and App. B.3 readout with a smoothed quantized residual. The append /
 // fold split follows fastpathlabs.ai research note 4, "What we built".
 //
-// One CTA (256 threads, 8 warps) owns one head-state. Work is bandwidth-bound
-// matvec plus rank-one terms, so it runs on the CUDA cores; no tensor cores.
+// One CTA owns one head-state. Work is bandwidth-bound matvec plus rank-one
+// terms, so it runs on the CUDA cores; no tensor cores.
+//
+// Data movement: right after reading the record count (or at once, when the
+// caller states the window phase), one thread issues bulk asynchronous copies
+// (cp.async.bulk, the TMA engine's 1-D form) of every byte the head-state needs
+// -- int8 codes, scales, compensators, buffered records, the token's q/k/v --
+// into shared memory on one mbarrier. All other arithmetic then reads shared
+// memory; global memory sees one burst of reads and the final writes. Waits on
+// the mbarrier are bounded (kWaitNs); on timeout the kernel records
+// LQ_ERR_TIMEOUT in the state's status word and leaves the head-state unchanged.
 //
 // Fixed evaluation order. Every value that feeds the stored state (u, decay
 // products, the per-entry fold chain, line scores, lambda, sigma, codes) is
@@ -26,6 +35,8 @@
 #include "lq_internal.h"
 
 namespace lqi {
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any wait for copies: 1 s
 
 // ---------------------------------------------------------------------------
 // small device helpers
@@ -79,7 +90,7 @@ __device__ __forceinline__ void load16(const float* src, float d[16]) {
   const float4* s4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    float4 x = s4[c];
+    const float4 x = s4[c];
     d[4 * c] = x.x;
     d[4 * c + 1] = x.y;
     d[4 * c + 2] = x.z;
@@ -97,35 +108,227 @@ __device__ __forceinline__ int sidx(int i, int j) {
   return (i << 7) + ((c ^ x) << 2) + (j & 3);
 }
 
-// Decay products, backward running products (no division):
-//   P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.
-// alpha_m for m < n_rec+1 comes from the record buffer; if `cur` is non-null it
-// is alpha_n (the token being appended). GDN: one scalar per m (thread 0).
-// KDA: one column chain per key channel (threads 0..127). P is [(n+1)][alen].
+// ---------------------------------------------------------------------------
+// bulk copies into shared memory on an mbarrier (inline PTX, sm_90+ forms)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// memory into this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` for at most kWaitNs; false on timeout.
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitNs) return false;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// staging layout: byte offsets into dynamic shared memory
+
+__host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+
+struct Stage {
+  int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, q, k, v, alpha_cur;
+  int y, aq, zk, zq, basek, baseq, P, g, h, ec, eq, ca, bd;
+  int end;
+};
+
+// `slots`: record slots staged (records held, plus one for the token being
+// appended when a fold follows). `append`: stage q/k/v and the append's work
+// vectors. `fold`: room for the expanded compensators.
+__host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots, bool append,
+                                              bool fold) {
+  Stage L;
+  int o = 0;
+  L.codes = o;
+  o += kD * kD;
+  L.sigma = o;
+  o += 4 * kD;
+  L.lambda = o;
+  o += 4 * kD;
+  L.comp_id = o;
+  o += al16(4 * comp_id_stride);
+  L.comp_line = o;
+  o += 4 * kD * C;
+  L.rec_k = o;
+  o += 4 * kD * slots;
+  L.rec_u = o;
+  o += 4 * kD * slots;
+  L.rec_alpha = o;
+  o += kda ? 4 * kD * slots : al16(4 * ((W + 3) / 4 * 4));
+  const int va = append ? 4 * kD : 0;
+  L.q = o;
+  o += va;
+  L.k = o;
+  o += va;
+  L.v = o;
+  o += va;
+  L.alpha_cur = o;
+  o += kda ? va : 0;
+  L.y = o;
+  o += va;
+  L.aq = o;
+  o += va;
+  L.zk = o;
+  o += va;
+  L.zq = o;
+  o += va;
+  L.basek = o;
+  o += va;
+  L.baseq = o;
+  o += va;
+  L.P = o;
+  o += al16(4 * (W + 1) * (kda ? kD : 1));
+  L.g = o;
+  o += al16(4 * (W + 1));
+  L.h = o;
+  o += al16(4 * (W + 1));
+  L.ec = o;
+  o += al16(4 * (C > 0 ? C : 1));
+  L.eq = o;
+  o += al16(4 * (C > 0 ? C : 1));
+  L.ca = o;
+  o += fold ? 4 * kD * C : 0;
+  L.bd = o;
+  o += fold ? 4 * kD * C : 0;
+  L.end = al16(o);
+  return L;
+}
+
+// Fold workspace after region R1 = max(64 KB state tile, staging), which holds
+// the staged inputs until the reconstruction has read them and the tile after.
+struct Tail {
+  float* rowpart;  // [8][128]  per-row block partials of the squared length
+  float* colpart;  // [8][128]  per-column block partials
+  float* score;    // [256]     line scores: rows 0..127, columns 128..255
+  float* gsc;      // [128]     1 / lambda
+  int* win;        // [4]
+};
+constexpr int kTileBytes = kD * kD * 4;
+constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + 128 + 4) * 4;
+
+__host__ __device__ inline int region1_bytes(const Stage& L) {
+  const int r = L.end > kTileBytes ? L.end : kTileBytes;
+  return (r + 127) & ~127;
+}
+
+__device__ __forceinline__ Tail carve_tail(char* base, int r1) {
+  Tail t;
+  float* x = reinterpret_cast<float*>(base + r1);
+  t.rowpart = x;
+  x += 8 * kD;
+  t.colpart = x;
+  x += 8 * kD;
+  t.score = x;
+  x += 256;
+  t.gsc = x;
+  x += 128;
+  t.win = reinterpret_cast<int*>(x);
+  return t;
+}
+
+template <typename T>
+__device__ __forceinline__ T* at(char* base, int off) {
+  return reinterpret_cast<T*>(base + off);
+}
+
+}  // namespace lqi
+
+namespace lqi {
+
+// ---------------------------------------------------------------------------
+// Staging: one thread issues every copy of head-state s (n0 records held) on
+// `bar`, with the exact byte count announced first.
+__device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, const Stage& L, char* sm,
+                                            uint64_t* bar, bool append) {
+  const uint32_t rec = 4u * kD * (uint32_t)n0;
+  const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
+  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + 2u * rec +
+                   alpha_bytes;
+  if (append) bytes += 12u * kD + (p.kda ? 4u * kD : 0u);
+  mbar_expect_tx(bar, bytes);
+  bulk_g2s(sm + L.codes, p.codes + s * (kD * kD), kD * kD, bar);
+  bulk_g2s(sm + L.sigma, p.sigma + s * kD, 4 * kD, bar);
+  bulk_g2s(sm + L.lambda, p.lambda + s * kD, 4 * kD, bar);
+  bulk_g2s(sm + L.comp_id, p.comp_id + s * p.comp_id_stride, 4u * (uint32_t)p.comp_id_stride, bar);
+  if (p.C > 0) bulk_g2s(sm + L.comp_line, p.comp_line + s * p.C * kD, 4u * kD * (uint32_t)p.C, bar);
+  if (n0 > 0) {
+    bulk_g2s(sm + L.rec_k, p.rec_k + s * p.W * kD, rec, bar);
+    bulk_g2s(sm + L.rec_u, p.rec_u + s * p.W * kD, rec, bar);
+  }
+  if (!p.kda)
+    bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
+  else if (n0 > 0)
+    bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
+  if (append) {
+    bulk_g2s(sm + L.q, p.q + s * kD, 4 * kD, bar);
+    bulk_g2s(sm + L.k, p.k + s * kD, 4 * kD, bar);
+    bulk_g2s(sm + L.v, p.v + s * kD, 4 * kD, bar);
+    if (p.kda) bulk_g2s(sm + L.alpha_cur, p.alpha + s * kD, 4 * kD, bar);
+  }
+}
+
+// Decay products from staged alphas (records 1..n-1, then alpha_n = `cur`, or
+// records 1..n when cur is null). Backward running products, no division:
+//   P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.  P is [(n+1)][alen].
 template <bool KDA>
-__device__ __forceinline__ void decay_products(const Params& p, int64_t s, int n, const float* cur, float* P) {
+__device__ __forceinline__ void decay_products(int n, const float* rec_alpha, const float* cur_vec, float cur_scalar,
+                                               bool have_cur, float* P) {
   const int tid = threadIdx.x;
   if (KDA) {
     if (tid < kD) {
-      const float* ra = p.rec_alpha + s * p.alpha_stride + tid;
       float pr = 1.0f;
       P[n * kD + tid] = pr;
       for (int m = n; m >= 1; --m) {
-        const float am = (cur && m == n) ? cur[tid] : ra[(m - 1) * kD];
+        const float am = (have_cur && m == n) ? cur_vec[tid] : rec_alpha[(m - 1) * kD + tid];
         pr = __fmul_rn(pr, am);
         P[(m - 1) * kD + tid] = pr;
       }
     }
-  } else {
-    if (tid == 0) {
-      const float* ra = p.rec_alpha + s * p.alpha_stride;
-      float pr = 1.0f;
-      P[n] = pr;
-      for (int m = n; m >= 1; --m) {
-        const float am = (cur && m == n) ? cur[0] : ra[m - 1];
-        pr = __fmul_rn(pr, am);
-        P[m - 1] = pr;
-      }
+  } else if (tid == 0) {
+    float pr = 1.0f;
+    P[n] = pr;
+    for (int m = n; m >= 1; --m) {
+      const float am = (have_cur && m == n) ? cur_scalar : rec_alpha[m - 1];
+      pr = __fmul_rn(pr, am);
+      P[m - 1] = pr;
     }
   }
 }
@@ -135,147 +338,133 @@ __device__ __forceinline__ float Pj(const float* P, int m, int j) {
   return KDA ? P[m * kD + j] : P[m];
 }
 
-}  // namespace lqi
-
-namespace lqi {
-
 // ---------------------------------------------------------------------------
-// Append (A0-A7): one token into one head-state that holds n-1 records.
-// LeapQuant §3.2 (outputs from the fixed low-bit state plus buffered records),
-// App. B.2 (base term O(d_k d_v), each record O(d_k + d_v)), App. B.3 (the
-// smoothing scales act on the residual term only), §3.3 (compensators are
-// records at window position 0 carrying the full decay A_n).
-
-// Vectors read as float4 come first; every array size is a multiple of 4 floats
-// so each member starts on a 16-byte boundary.
-template <bool KDA>
-struct alignas(16) AppendSmem {
-  float kn[kD], qn[kD];                                 // current token's k, q
-  float y[kD], aq[kD];                                  // A_n . k_n and A_n . q_n
-  float zk[kD], zq[kD];                                 // lambda . y, lambda . (A_n . q_n)
-  float basek[kD], baseq[kD];                           // sigma_i * dot(Cd[i,:], z)
-  float P[((kMaxW + 1) * (KDA ? kD : 1) + 3) / 4 * 4];  // decay products P_m, m = 0..n
-  float g[(kMaxW + 1 + 3) / 4 * 4];                     // record reads k_m . (P_m . k_n)
-  float h[(kMaxW + 1 + 3) / 4 * 4];                     // output terms k_m . (P_m . q_n)
-  float ec[kMaxC], eq[kMaxC];                           // compensator reads b_c . y, b_c . (A_n . q_n)
-};
-static_assert(offsetof(AppendSmem<false>, zk) % 16 == 0 && offsetof(AppendSmem<false>, zq) % 16 == 0,
-              "float4 loads of z need 16-byte alignment");
-static_assert(offsetof(AppendSmem<true>, zk) % 16 == 0 && sizeof(AppendSmem<false>) % 16 == 0 &&
-                  sizeof(AppendSmem<true>) % 16 == 0,
-              "dynamic shared memory after AppendSmem stays 16-byte aligned");
-
-template <bool KDA>
-__device__ __forceinline__ void append_body(const Params& p, int64_t s, int n, AppendSmem<KDA>& sm) {
+// Append (A0-A7): one token into head-state s holding n-1 records, all inputs
+// staged in shared memory. LeapQuant §3.2 (outputs from the fixed low-bit state
+// plus buffered records), App. B.2 (base term O(d_k d_v), each record
+// O(d_k + d_v)), App. B.3 (the smoothing scales act on the residual term only),
+// §3.3 (compensators are records at window position 0 carrying the full decay).
+// With `fold_follows`, the new record is also left in the staged buffers.
+template <bool KDA, int NT>
+__device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
+                                               float alpha_scalar, float beta, bool fold_follows) {
+  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
   const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
-  const float* alpha_cur = KDA ? p.alpha + s * kD : p.alpha + s;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float* P = at<float>(sm, L.P);
+  float* rk = at<float>(sm, L.rec_k);
+  float* ru = at<float>(sm, L.rec_u);
+  const float* kn = at<float>(sm, L.k);
+  const float* qn = at<float>(sm, L.q);
+  float* y = at<float>(sm, L.y);
+  float* aq = at<float>(sm, L.aq);
+  float* zk = at<float>(sm, L.zk);
+  float* zq = at<float>(sm, L.zq);
+  float* basek = at<float>(sm, L.basek);
+  float* baseq = at<float>(sm, L.baseq);
+  float* g = at<float>(sm, L.g);
+  float* h = at<float>(sm, L.h);
+  float* ec = at<float>(sm, L.ec);
+  float* eq = at<float>(sm, L.eq);
+  const float* sg = at<float>(sm, L.sigma);
+  const float* lam = at<float>(sm, L.lambda);
+  const int32_t* cid = at<int32_t>(sm, L.comp_id);
+  const float* cl = at<float>(sm, L.comp_line);
 
   // A0: decay products over records 1..n-1 and this token's alpha.
-  decay_products<KDA>(p, s, n, alpha_cur, sm.P);
-  if (tid < kD)
-    sm.kn[tid] = p.k[s * kD + tid];
-  else
-    sm.qn[tid - kD] = p.q[s * kD + tid - kD];
+  decay_products<KDA>(n, at<float>(sm, L.rec_alpha), at<float>(sm, L.alpha_cur), alpha_scalar, true, P);
   __syncthreads();
 
   // A1: y = A_n . k_n; z = lambda . y (and the same for q, for the output).
   if (tid < kD) {
     const int j = tid;
-    const float A = Pj<KDA>(sm.P, 0, j);
-    const float lam = p.lambda[s * kD + j];
-    const float y = __fmul_rn(A, sm.kn[j]);
-    const float aq = __fmul_rn(A, sm.qn[j]);
-    sm.y[j] = y;
-    sm.aq[j] = aq;
-    sm.zk[j] = __fmul_rn(lam, y);
-    sm.zq[j] = __fmul_rn(lam, aq);
+    const float A = Pj<KDA>(P, 0, j);
+    const float yy = __fmul_rn(A, kn[j]);
+    const float qa = __fmul_rn(A, qn[j]);
+    y[j] = yy;
+    aq[j] = qa;
+    zk[j] = __fmul_rn(lam[j], yy);
+    zq[j] = __fmul_rn(lam[j], qa);
   }
   __syncthreads();
 
   // A2: fused dequantize + two matvecs. Lane group (w, r) owns rows
-  // 32pp + 4w + r; lane qq owns the 16-code block 16qq..16qq+15 of each row:
-  // one 16-byte load, 16 exact conversions, 2 fmas per code, then the tree.
+  // pp * 4 * NW + 4w + r; lane qq owns the 16-code block 16qq..16qq+15 of each
+  // row: one 16-byte load, 16 exact conversions, 2 fmas per code, the tree.
   {
-    float zk[16], zq[16];
-    load16(sm.zk + 16 * qq, zk);
-    load16(sm.zq + 16 * qq, zq);
-    const int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
-    int4 cw[4];
+    float zkr[16], zqr[16];
+    load16(zk + 16 * qq, zkr);
+    load16(zq + 16 * qq, zqr);
+    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) cw[pp] = *reinterpret_cast<const int4*>(cbase + (32 * pp + 4 * w + r) * kD);
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int i = 32 * pp + 4 * w + r;
+    for (int pp = 0; pp < RPT; ++pp) {
+      const int i = pp * 4 * NW + 4 * w + r;
       float f[16];
-      codes16_to_float(cw[pp], f);
-      float ak = 0.0f, aq = 0.0f;
+      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
+      float ak = 0.0f, aqq = 0.0f;
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        ak = __fmaf_rn(f[t], zk[t], ak);
-        aq = __fmaf_rn(f[t], zq[t], aq);
+        ak = __fmaf_rn(f[t], zkr[t], ak);
+        aqq = __fmaf_rn(f[t], zqr[t], aqq);
       }
       ak = tree8(ak);
-      aq = tree8(aq);
+      aqq = tree8(aqq);
       if (qq == 0) {
-        const float sg = p.sigma[s * kD + i];
-        sm.basek[i] = __fmul_rn(sg, ak);
-        sm.baseq[i] = __fmul_rn(sg, aq);
+        basek[i] = __fmul_rn(sg[i], ak);
+        baseq[i] = __fmul_rn(sg[i], aqq);
       }
     }
   }
 
-  // A3/A4 reads, one lane group (8 lanes) per dot product: records m = 1..n-1,
-  // then compensators, then k_n . q_n (the new record's output term, P_n = 1).
+  // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
+  // compensators, then k_n . q_n (the new record's output term, P_n = 1).
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
     const int njobs = nrec + p.C + 1;
-    for (int base = 0; base < njobs; base += kThreads / 8) {
+    for (int base = 0; base < njobs; base += NT / 8) {
       const int job = base + grp;
       float pa = 0.0f, pb = 0.0f;
       if (job < njobs) {
         if (job < nrec) {
           const int m = job + 1;
-          float kv[16];
-          load16(p.rec_k + (s * p.W + (m - 1)) * kD + 16 * qq, kv);
+          float kv[16], kx[16], qx[16];
+          load16(rk + (m - 1) * kD + 16 * qq, kv);
+          load16(kn + 16 * qq, kx);
+          load16(qn + 16 * qq, qx);
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            const int j = 16 * qq + t;
-            const float Pm = Pj<KDA>(sm.P, m, j);
-            pa = __fmaf_rn(kv[t], __fmul_rn(Pm, sm.kn[j]), pa);
-            pb = __fmaf_rn(kv[t], __fmul_rn(Pm, sm.qn[j]), pb);
+            const float Pm = Pj<KDA>(P, m, 16 * qq + t);
+            pa = __fmaf_rn(kv[t], __fmul_rn(Pm, kx[t]), pa);
+            pb = __fmaf_rn(kv[t], __fmul_rn(Pm, qx[t]), pb);
           }
         } else if (job < nrec + p.C) {
           const int c = job - nrec;
-          const int id = p.comp_id[s * p.comp_id_stride + c];
-          const float* line = p.comp_line + (s * p.C + c) * kD;
+          const int id = cid[c];
+          const float* line = cl + c * kD;
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const int j = 16 * qq + t;
             const float b = (id < kD) ? line[j] : (j == id - kD ? 1.0f : 0.0f);
-            pa = __fmaf_rn(b, sm.y[j], pa);
-            pb = __fmaf_rn(b, sm.aq[j], pb);
+            pa = __fmaf_rn(b, y[j], pa);
+            pb = __fmaf_rn(b, aq[j], pb);
           }
         } else {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int j = 16 * qq + t;
-            pb = __fmaf_rn(sm.kn[j], sm.qn[j], pb);
-          }
+          for (int t = 0; t < 16; ++t) pb = __fmaf_rn(kn[16 * qq + t], qn[16 * qq + t], pb);
         }
       }
       pa = tree8(pa);
       pb = tree8(pb);
       if (job < njobs && qq == 0) {
         if (job < nrec) {
-          sm.g[job + 1] = pa;
-          sm.h[job + 1] = pb;
+          g[job + 1] = pa;
+          h[job + 1] = pb;
         } else if (job < nrec + p.C) {
-          sm.ec[job - nrec] = pa;
-          sm.eq[job - nrec] = pb;
+          ec[job - nrec] = pa;
+          eq[job - nrec] = pb;
         } else {
-          sm.h[n] = pb;
+          h[n] = pb;
         }
       }
     }
@@ -284,33 +473,35 @@ __device__ __forceinline__ void append_body(const Params& p, int64_t s, int n, A
 
   // A3-A5 per value row: acc = base; compensators in order; records in order;
   // u_n = beta (v - acc). A6: the output in any order. A7: store record n.
+  const float* vv = at<float>(sm, L.v);
   if (tid < kD) {
     const int i = tid;
-    float acc = sm.basek[i];
-    float oo = sm.baseq[i];
+    float acc = basek[i];
+    float oo = baseq[i];
     for (int c = 0; c < p.C; ++c) {
-      const int id = p.comp_id[s * p.comp_id_stride + c];
-      const float a = (id < kD) ? (i == id ? 1.0f : 0.0f) : p.comp_line[(s * p.C + c) * kD + i];
-      acc = __fmaf_rn(a, sm.ec[c], acc);
-      oo = __fmaf_rn(a, sm.eq[c], oo);
+      const int id = cid[c];
+      const float a = (id < kD) ? (i == id ? 1.0f : 0.0f) : cl[c * kD + i];
+      acc = __fmaf_rn(a, ec[c], acc);
+      oo = __fmaf_rn(a, eq[c], oo);
     }
-    const float* ru = p.rec_u + s * p.W * kD + i;
     for (int m = 1; m <= n - 1; ++m) {
-      const float um = ru[(m - 1) * kD];
-      acc = __fmaf_rn(um, sm.g[m], acc);
-      oo = __fmaf_rn(um, sm.h[m], oo);
+      const float um = ru[(m - 1) * kD + i];
+      acc = __fmaf_rn(um, g[m], acc);
+      oo = __fmaf_rn(um, h[m], oo);
     }
-    const float u = __fmul_rn(p.beta[s], __fsub_rn(p.v[s * kD + i], acc));
-    oo = __fmaf_rn(u, sm.h[n], oo);
+    const float u = __fmul_rn(beta, __fsub_rn(vv[i], acc));
+    oo = __fmaf_rn(u, h[n], oo);
     p.rec_u[(s * p.W + (n - 1)) * kD + i] = u;
     p.o[s * kD + i] = oo;
-  } else {
+    if (fold_follows) ru[(n - 1) * kD + i] = u;
+  } else if (tid < 2 * kD) {
     const int j = tid - kD;
-    p.rec_k[(s * p.W + (n - 1)) * kD + j] = sm.kn[j];
+    p.rec_k[(s * p.W + (n - 1)) * kD + j] = kn[j];
+    if (fold_follows) rk[(n - 1) * kD + j] = kn[j];
     if (KDA)
-      p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + j] = p.alpha[s * kD + j];
+      p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + j] = at<float>(sm, L.alpha_cur)[j];
     else if (j == 0)
-      p.rec_alpha[s * p.alpha_stride + (n - 1)] = p.alpha[s];
+      p.rec_alpha[s * p.alpha_stride + (n - 1)] = alpha_scalar;
   }
 }
 
@@ -323,145 +514,145 @@ namespace lqi {
 // coordinates at the window boundary; §3.3: compensators are the largest
 // outlier lines kept in fp32; §3.4: per-key-channel smoothing scales
 // sqrt(mean |.|) with a floor; then one rounding to int8 per row step.
-// The state lives in shared memory as a swizzled 128x128 fp32 tile (64 KB).
 
-struct FoldSmem {
-  float* S;        // [128*128] swizzled
-  float* kd;       // [W][128]  P_m . k_m
-  float* U;        // [W][128]  u_m
-  float* ca;       // [C][128]  expanded a_c
-  float* bd;       // [C][128]  P_0 . b_c
-  float* P;        // [(W+1)][alen]
-  float* rowpart;  // [8][128]  per-row block partials of the squared length
-  float* colpart;  // [8][128]  per-column block partials
-  float* score;    // [256]     line scores: rows 0..127, columns 128..255
-  float* gsc;      // [128]     1 / lambda
-  int* win;        // [4]
-};
-
-__host__ __device__ inline size_t fold_smem_floats(int W, int C, int kda) {
-  const size_t alen = kda ? kD : 1;
-  const size_t ptab = (((size_t)(W + 1) * alen) + 3) / 4 * 4;
-  return (size_t)kD * kD + 2 * (size_t)W * kD + 2 * (size_t)C * kD + ptab + 2 * 8 * kD + 256 + 128 + 4;
-}
-
-__device__ __forceinline__ FoldSmem carve(float* base, int W, int C, int kda) {
-  FoldSmem f;
-  const size_t alen = kda ? kD : 1;
-  float* x = base;
-  f.S = x;        x += kD * kD;
-  f.kd = x;       x += (size_t)W * kD;
-  f.U = x;        x += (size_t)W * kD;
-  f.ca = x;       x += (size_t)C * kD;
-  f.bd = x;       x += (size_t)C * kD;
-  f.P = x;        x += (((size_t)(W + 1) * alen) + 3) / 4 * 4;
-  f.rowpart = x;  x += 8 * kD;
-  f.colpart = x;  x += 8 * kD;
-  f.score = x;    x += 256;
-  f.gsc = x;      x += 128;
-  f.win = reinterpret_cast<int*>(x);
-  return f;
-}
-
-// F0: tables for the reconstruction of a head-state holding n records.
-template <bool KDA>
-__device__ __forceinline__ void fold_tables(const Params& p, int64_t s, int n, const FoldSmem& fs) {
+// F0: record keys scaled by their decay products, in place over the staged keys
+// (kd_m = P_m . k_m), and the expanded compensators (a_c, P_0 . b_c).
+template <bool KDA, int NT>
+__device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage& L, char* sm) {
   const int tid = threadIdx.x;
-  decay_products<KDA>(p, s, n, nullptr, fs.P);
-  __syncthreads();
-  for (int e = tid; e < n * kD; e += kThreads) {
+  const float* P = at<float>(sm, L.P);
+  float* rk = at<float>(sm, L.rec_k);
+  for (int e = tid; e < n * kD; e += NT) {
     const int m1 = e >> 7, j = e & (kD - 1);
-    const size_t off = (size_t)(s * p.W + m1) * kD + j;
-    fs.kd[e] = __fmul_rn(Pj<KDA>(fs.P, m1 + 1, j), p.rec_k[off]);
-    fs.U[e] = p.rec_u[off];
+    rk[e] = __fmul_rn(Pj<KDA>(P, m1 + 1, j), rk[e]);
   }
-  for (int e = tid; e < p.C * kD; e += kThreads) {
+  const int32_t* cid = at<int32_t>(sm, L.comp_id);
+  const float* cl = at<float>(sm, L.comp_line);
+  float* ca = at<float>(sm, L.ca);
+  float* bd = at<float>(sm, L.bd);
+  for (int e = tid; e < p.C * kD; e += NT) {
     const int c = e >> 7, x = e & (kD - 1);
-    const int id = p.comp_id[s * p.comp_id_stride + c];
-    const float lv = p.comp_line[(s * p.C + c) * kD + x];
+    const int id = cid[c];
+    const float lv = cl[c * kD + x];
     const float a = (id < kD) ? (x == id ? 1.0f : 0.0f) : lv;
     const float b = (id < kD) ? lv : (x == id - kD ? 1.0f : 0.0f);
-    fs.ca[e] = a;
-    fs.bd[e] = __fmul_rn(Pj<KDA>(fs.P, 0, x), b);
+    ca[e] = a;
+    bd[e] = __fmul_rn(Pj<KDA>(P, 0, x), b);
   }
   __syncthreads();
 }
 
-// F1 for the 4 rows x 16 columns a thread owns (rows 32pp + 4w + r, columns
-// 16qq..16qq+15): S_ij = ((sigma_i Cd_ij) lambda_j) P_0[j], then the compensators
-// in order, then the records in order, each an fma.
-template <bool KDA>
-__device__ __forceinline__ void reconstruct_rows(const Params& p, int64_t s, int n, const FoldSmem& fs,
-                                                 float acc[4][16]) {
+// F1 for the RPT rows x 16 columns a thread owns (rows pp*4*NW + 4w + r,
+// columns 16qq..16qq+15): S_ij = ((sigma_i Cd_ij) lambda_j) P_0[j], then the
+// compensators in order, then the records in order, each an fma.
+template <bool KDA, int NT>
+__device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm,
+                                                 float acc[][16]) {
+  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
   const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  const float* P = at<float>(sm, L.P);
+  const float* sg = at<float>(sm, L.sigma);
+  const float* ca = at<float>(sm, L.ca);
+  const float* bd = at<float>(sm, L.bd);
+  const float* kd = at<float>(sm, L.rec_k);
+  const float* U = at<float>(sm, L.rec_u);
   float lam[16], p0[16];
-  load16(p.lambda + s * kD + 16 * qq, lam);
+  load16(at<float>(sm, L.lambda) + 16 * qq, lam);
+  if (KDA) {
+    load16(P + 16 * qq, p0);
+  } else {
 #pragma unroll
-  for (int t = 0; t < 16; ++t) p0[t] = Pj<KDA>(fs.P, 0, 16 * qq + t);
-  const int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
+    for (int t = 0; t < 16; ++t) p0[t] = P[0];
+  }
+  const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
 #pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-    const int i = 32 * pp + 4 * w + r;
-    const float sg = p.sigma[s * kD + i];
+  for (int pp = 0; pp < RPT; ++pp) {
+    const int i = pp * 4 * NW + 4 * w + r;
+    const float s_i = sg[i];
     float f[16];
-    codes16_to_float(*reinterpret_cast<const int4*>(cbase + i * kD), f);
+    codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
 #pragma unroll
-    for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(sg, f[t]), lam[t]), p0[t]);
+    for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[t]), lam[t]), p0[t]);
   }
   for (int c = 0; c < p.C; ++c) {
     float b[16];
-    load16(fs.bd + c * kD + 16 * qq, b);
+    load16(bd + c * kD + 16 * qq, b);
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const float a = fs.ca[c * kD + 32 * pp + 4 * w + r];
+    for (int pp = 0; pp < RPT; ++pp) {
+      const float a = ca[c * kD + pp * 4 * NW + 4 * w + r];
 #pragma unroll
       for (int t = 0; t < 16; ++t) acc[pp][t] = __fmaf_rn(a, b[t], acc[pp][t]);
     }
   }
   for (int m = 0; m < n; ++m) {
     float kdv[16];
-    load16(fs.kd + m * kD + 16 * qq, kdv);
+    load16(kd + m * kD + 16 * qq, kdv);
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const float u = fs.U[m * kD + 32 * pp + 4 * w + r];
+    for (int pp = 0; pp < RPT; ++pp) {
+      const float u = U[m * kD + pp * 4 * NW + 4 * w + r];
 #pragma unroll
       for (int t = 0; t < 16; ++t) acc[pp][t] = __fmaf_rn(u, kdv[t], acc[pp][t]);
     }
   }
 }
 
-// F2-F6 on the state tile already in fs.S, with row partials and row scores
-// already in fs.rowpart / fs.score[0..127].
-__device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, const FoldSmem& fs) {
+// Store a thread's rows into the swizzled tile S and record their row
+// partials and row scores (squared lengths).
+template <int NT>
+__device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float acc[][16]) {
+  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
   const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+#pragma unroll
+  for (int pp = 0; pp < RPT; ++pp) {
+    const int i = pp * 4 * NW + 4 * w + r;
+    float pr = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) pr = __fmaf_rn(acc[pp][t], acc[pp][t], pr);
+    tl.rowpart[qq * kD + i] = pr;
+    const float rho = tree8(pr);
+    if (qq == 0) tl.score[i] = rho;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+      *reinterpret_cast<float4*>(&S[sidx(i, 16 * qq + 4 * c4)]) =
+          make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
+  }
+  __syncthreads();
+}
+
+// F2-F6 on the state tile S, with row partials and row scores in the tail.
+template <int NT>
+__device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
+  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 
   // Column scores: block partial b of column j is an fma chain over rows 16b..16b+15.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) {
+    for (int b = tid >> 7; b < 8; b += NT / kD) {
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
       float pc = 0.0f;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float x = fs.S[sidx(16 * b + t, j)];
-        pc = __fmaf_rn(x, x, pc);
-      }
-      fs.colpart[b * kD + j] = pc;
+      for (int t = 0; t < 16; ++t) pc = __fmaf_rn(x[t], x[t], pc);
+      tl.colpart[b * kD + j] = pc;
     }
   }
   __syncthreads();
-  if (tid < kD) fs.score[kD + tid] = tree8_mem(fs.colpart + tid, kD);
+  if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
 
   // F2: C greedy rounds of the longest line, ties to the smallest id.
   for (int c = 0; c < p.C; ++c) {
     if (tid < 32) {
-      float bv = fs.score[8 * tid];
+      float bv = tl.score[8 * tid];
       int bi = 8 * tid;
 #pragma unroll
       for (int e = 1; e < 8; ++e) {
-        const float v = fs.score[8 * tid + e];
+        const float v = tl.score[8 * tid + e];
         if (v > bv) {
           bv = v;
           bi = 8 * tid + e;
@@ -477,55 +668,55 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, c
         }
       }
       if (tid == 0) {
-        fs.win[0] = bi;
+        tl.win[0] = bi;
         p.comp_id[s * p.comp_id_stride + c] = bi;
       }
     }
     __syncthreads();
-    const int win = fs.win[0];
+    const int win = tl.win[0];
     float* line = p.comp_line + (s * p.C + c) * kD;
     if (win < kD) {
       // Row win: copy, zero, refresh the column partials of its row block.
       if (tid < kD) {
         const int j = tid;
-        float* e = &fs.S[sidx(win, j)];
+        float* e = &S[sidx(win, j)];
         line[j] = *e;
         *e = 0.0f;
         const int b = win >> 4;
+        float x[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
         float pc = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float x = fs.S[sidx(16 * b + t, j)];
-          pc = __fmaf_rn(x, x, pc);
-        }
-        fs.colpart[b * kD + j] = pc;
-        fs.score[kD + j] = tree8_mem(fs.colpart + j, kD);
+        for (int t = 0; t < 16; ++t) pc = __fmaf_rn(x[t], x[t], pc);
+        tl.colpart[b * kD + j] = pc;
+        tl.score[kD + j] = tree8_mem(tl.colpart + j, kD);
       } else if (tid < kD + 8) {
-        fs.rowpart[(tid - kD) * kD + win] = 0.0f;
+        tl.rowpart[(tid - kD) * kD + win] = 0.0f;
       } else if (tid == kD + 8) {
-        fs.score[win] = 0.0f;
+        tl.score[win] = 0.0f;
       }
     } else {
       // Column js: copy, zero, refresh the row partials of its column block.
       const int js = win - kD;
       if (tid < kD) {
         const int i = tid;
-        float* e = &fs.S[sidx(i, js)];
+        float* e = &S[sidx(i, js)];
         line[i] = *e;
         *e = 0.0f;
         const int q = js >> 4;
+        float x[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) x[t] = S[sidx(i, 16 * q + t)];
         float pr = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float x = fs.S[sidx(i, 16 * q + t)];
-          pr = __fmaf_rn(x, x, pr);
-        }
-        fs.rowpart[q * kD + i] = pr;
-        fs.score[i] = tree8_mem(fs.rowpart + i, kD);
+        for (int t = 0; t < 16; ++t) pr = __fmaf_rn(x[t], x[t], pr);
+        tl.rowpart[q * kD + i] = pr;
+        tl.score[i] = tree8_mem(tl.rowpart + i, kD);
       } else if (tid < kD + 8) {
-        fs.colpart[(tid - kD) * kD + js] = 0.0f;
+        tl.colpart[(tid - kD) * kD + js] = 0.0f;
       } else if (tid == kD + 8) {
-        fs.score[win] = 0.0f;
+        tl.score[win] = 0.0f;
       }
     }
     __syncthreads();
@@ -534,34 +725,37 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, c
   // F3: smoothing scales from the residual's column sums of |R|.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) {
+    for (int b = tid >> 7; b < 8; b += NT / kD) {
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
       float pa = 0.0f;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) pa = __fadd_rn(pa, fabsf(fs.S[sidx(16 * b + t, j)]));
-      fs.colpart[b * kD + j] = pa;
+      for (int t = 0; t < 16; ++t) pa = __fadd_rn(pa, fabsf(x[t]));
+      tl.colpart[b * kD + j] = pa;
     }
   }
   __syncthreads();
   if (tid < kD) {
-    const float mu = __fmul_rn(tree8_mem(fs.colpart + tid, kD), 1.0f / (float)kD);
+    const float mu = __fmul_rn(tree8_mem(tl.colpart + tid, kD), 1.0f / (float)kD);
     const float lam = p.smooth ? fmaxf(__fsqrt_rn(mu), p.lambda_floor) : 1.0f;
     p.lambda[s * kD + tid] = lam;
-    fs.gsc[tid] = __fdiv_rn(1.0f, lam);
+    tl.gsc[tid] = __fdiv_rn(1.0f, lam);
   }
   __syncthreads();
 
   // F4-F5: per-row absmax of t = R / lambda, one reciprocal per row, round once.
   {
     float g[16];
-    load16(fs.gsc + 16 * qq, g);
+    load16(tl.gsc + 16 * qq, g);
     int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int i = 32 * pp + 4 * w + r;
+    for (int pp = 0; pp < RPT; ++pp) {
+      const int i = pp * 4 * NW + 4 * w + r;
       float t[16];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const float4 x = *reinterpret_cast<const float4*>(&fs.S[sidx(i, 16 * qq + 4 * c4)]);
+        const float4 x = *reinterpret_cast<const float4*>(&S[sidx(i, 16 * qq + 4 * c4)]);
         t[4 * c4 + 0] = x.x;
         t[4 * c4 + 1] = x.y;
         t[4 * c4 + 2] = x.z;
@@ -574,16 +768,16 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, c
         mx = fmaxf(mx, fabsf(t[e]));
       }
       mx = max8(mx);
-      float sg = 0.0f, h = 0.0f;
+      float sgm = 0.0f, hh = 0.0f;
       if (mx != 0.0f) {
-        sg = __fdiv_rn(mx, 127.0f);
-        h = __fdiv_rn(127.0f, mx);
+        sgm = __fdiv_rn(mx, 127.0f);
+        hh = __fdiv_rn(127.0f, mx);
       }
-      if (qq == 0) p.sigma[s * kD + i] = sg;
+      if (qq == 0) p.sigma[s * kD + i] = sgm;
       uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        int cq = __float2int_rn(__fmul_rn(t[e], h));
+        int cq = __float2int_rn(__fmul_rn(t[e], hh));
         cq = min(max(cq, -127), 127);
         wd[e >> 2] |= ((uint32_t)cq & 0xFFu) << (8 * (e & 3));
       }
@@ -594,110 +788,157 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, c
   if (tid == 0) p.counts[s] = 0;
 }
 
-// Store a thread's 4x16 block into the tile and record its row partials/scores.
-__device__ __forceinline__ void tile_store_rows(const FoldSmem& fs, float acc[4][16]) {
-  const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
-#pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-    const int i = 32 * pp + 4 * w + r;
-    float pr = 0.0f;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) pr = __fmaf_rn(acc[pp][t], acc[pp][t], pr);
-    fs.rowpart[qq * kD + i] = pr;
-    const float rho = tree8(pr);
-    if (qq == 0) fs.score[i] = rho;
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4)
-      *reinterpret_cast<float4*>(&fs.S[sidx(i, 16 * qq + 4 * c4)]) =
-          make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
-  }
-  __syncthreads();
-}
+}  // namespace lqi
 
-template <bool KDA>
-__device__ __forceinline__ void fold_from_records(const Params& p, int64_t s, int n, float* dsm) {
-  const FoldSmem fs = carve(dsm, p.W, p.C, KDA);
-  fold_tables<KDA>(p, s, n, fs);
-  float acc[4][16];
-  reconstruct_rows<KDA>(p, s, n, fs, acc);
-  tile_store_rows(fs, acc);
-  boundary_from_tile(p, s, fs);
-}
+namespace lqi {
 
 // ---------------------------------------------------------------------------
 // kernels: one CTA per head-state
 
-extern __shared__ __align__(16) float lq_dyn_smem[];
+extern __shared__ __align__(128) char lq_dyn_smem[];
 
-__device__ __forceinline__ bool prologue(const Params& p, int64_t s, int& n0) {
-  if (!header_ok(p)) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
-    return false;
+// Thread 0 starts the copies (at once when `known_n0` >= 0, else after reading
+// the record count); every thread reads the header and count meanwhile. Then
+// every thread waits, boundedly, for the copies. Returns the record count held
+// (>= 0) or -1 after recording an error; the result is uniform over the CTA.
+__device__ __forceinline__ int stage_and_check(const Params& p, int64_t s, int known_n0, const Stage& L,
+                                               uint64_t* bar, int* s_issued, bool append, int max_n0) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    int n0 = known_n0;
+    if (n0 < 0) {
+      const int c = p.counts[s];
+      n0 = (c >= 0 && c <= max_n0) ? c : -1;
+    }
+    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append);
+    *s_issued = n0;
   }
-  n0 = p.counts[s];
-  if (n0 < 0 || n0 > p.W) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
-    return false;
+  const bool hdr = header_ok(p);
+  const int cnt = p.counts[s];
+  __syncthreads();
+  const int n0 = *s_issued;
+  if (n0 >= 0) {
+    bool ok = mbar_wait_bounded(bar, 0);
+    if (__syncthreads_or(!ok)) {
+      if (!ok) (void)mbar_wait_bounded(bar, 0);  // one more bounded chance for copies in flight
+      if (tid == 0) set_error(p, LQ_ERR_TIMEOUT, s);
+      return -1;
+    }
   }
-  return true;
+  int err = 0;
+  if (!hdr || cnt < 0 || cnt > p.W)
+    err = LQ_ERR_STATE;
+  else if (p.phase >= 0 && append && cnt != p.phase)
+    err = LQ_ERR_PHASE;
+  else if (append && cnt >= p.W)
+    err = LQ_ERR_WINDOW_FULL;
+  else if (cnt != n0)
+    err = LQ_ERR_STATE;
+  if (err) {
+    if (tid == 0) set_error(p, err, s);
+    return -1;
+  }
+  return cnt;
 }
 
+// Append only (no fold): the W-1 decode steps that cannot fill the window, and lq_append.
 template <bool KDA>
-__global__ void __launch_bounds__(kThreads) k_append(Params p) {
-  __shared__ __align__(16) AppendSmem<KDA> sm;
+__global__ void __launch_bounds__(256, 5) k_append(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  int n0;
-  if (!prologue(p, s, n0)) return;
-  if (p.phase >= 0 && n0 != p.phase) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_PHASE, s);
-    return;
-  }
-  if (n0 >= p.W) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_WINDOW_FULL, s);
-    return;
-  }
-  append_body<KDA>(p, s, n0 + 1, sm);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W - 1, true, false);
+  const float beta = p.beta[s];
+  const float alpha_s = KDA ? 0.0f : p.alpha[s];
+  const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
+  const int n0 = stage_and_check(p, s, known, L, &bar, &s_issued, true, p.W - 1);
+  if (n0 < 0) return;
+  append_compute<KDA, 256>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
+// Append, then -- when that fills the window -- fold while the state is on chip.
 template <bool KDA>
-__global__ void __launch_bounds__(kThreads) k_step(Params p) {
-  __shared__ __align__(16) AppendSmem<KDA> sm;
+__global__ void __launch_bounds__(512, 2) k_step(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  int n0;
-  if (!prologue(p, s, n0)) return;
-  if (p.phase >= 0 && n0 != p.phase) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_PHASE, s);
-    return;
-  }
-  if (n0 >= p.W) {
-    if (threadIdx.x == 0) set_error(p, LQ_ERR_WINDOW_FULL, s);
-    return;
-  }
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, true, true);
+  const float beta = p.beta[s];
+  const float alpha_s = KDA ? 0.0f : p.alpha[s];
+  const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
+  const int n0 = stage_and_check(p, s, known, L, &bar, &s_issued, true, p.W - 1);
+  if (n0 < 0) return;
   const int n = n0 + 1;
-  append_body<KDA>(p, s, n, sm);
+  append_compute<KDA, 512>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
   if (n < p.W) {
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  __syncthreads();  // record n is in global memory and visible to the whole CTA
-  fold_from_records<KDA>(p, s, n, lq_dyn_smem);
+  __syncthreads();
+  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
+  float acc[2][16];
+  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+  __syncthreads();  // every staged input has been read: the tile may overwrite them
+  const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
+  float* S = reinterpret_cast<float*>(lq_dyn_smem);
+  tile_store_rows<512>(S, tl, acc);
+  boundary_from_tile<512>(p, s, S, tl);
 }
 
+// Fold with the records held (any count 0..W): lq_fold.
 template <bool KDA>
-__global__ void __launch_bounds__(kThreads) k_fold(Params p) {
+__global__ void __launch_bounds__(512, 2) k_fold(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  int n0;
-  if (!prologue(p, s, n0)) return;
-  fold_from_records<KDA>(p, s, n0, lq_dyn_smem);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, false, true);
+  const int n = stage_and_check(p, s, -1, L, &bar, &s_issued, false, p.W);
+  if (n < 0) return;
+  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P));
+  __syncthreads();
+  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
+  float acc[2][16];
+  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+  __syncthreads();
+  const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
+  float* S = reinterpret_cast<float*>(lq_dyn_smem);
+  tile_store_rows<512>(S, tl, acc);
+  boundary_from_tile<512>(p, s, S, tl);
+}
+
+// The state each head-state stands for (F0-F1, no rounding): lq_export_state.
+template <bool KDA>
+__global__ void __launch_bounds__(512, 2) k_export(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_issued;
+  const int64_t s = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, false, true);
+  const int n = stage_and_check(p, s, -1, L, &bar, &s_issued, false, p.W);
+  if (n < 0) return;
+  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P));
+  __syncthreads();
+  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
+  float acc[2][16];
+  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    const int i = pp * 64 + 4 * w + r;
+    float4* dst = reinterpret_cast<float4*>(p.S_out + (s * kD + i) * kD + 16 * qq);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+      dst[c4] = make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
+  }
 }
 
 // Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
-__global__ void __launch_bounds__(kThreads) k_init(Params p) {
+__global__ void __launch_bounds__(512, 2) k_init(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   if (s == 0 && tid == 0) {
     p.hdr->magic = kMagic;
     p.hdr->version = kLayoutVersion;
@@ -707,11 +948,10 @@ __global__ void __launch_bounds__(kThreads) k_init(Params p) {
     p.hdr->reserved0 = 0;
     p.hdr->bad_state = -1;
   }
-  const FoldSmem fs = carve(lq_dyn_smem, p.W, p.C, p.kda);
-  float acc[4][16];
+  float acc[2][16];
 #pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-    const int i = 32 * pp + 4 * w + r;
+  for (int pp = 0; pp < 2; ++pp) {
+    const int i = pp * 64 + 4 * w + r;
     if (p.S0) {
       load16(p.S0 + (s * kD + i) * kD + 16 * qq, acc[pp]);
     } else {
@@ -719,67 +959,53 @@ __global__ void __launch_bounds__(kThreads) k_init(Params p) {
       for (int t = 0; t < 16; ++t) acc[pp][t] = 0.0f;
     }
   }
-  tile_store_rows(fs, acc);
-  boundary_from_tile(p, s, fs);
-}
-
-template <bool KDA>
-__global__ void __launch_bounds__(kThreads) k_export(Params p) {
-  const int64_t s = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int w = tid >> 5, l = tid & 31, r = l >> 3, qq = l & 7;
-  int n0;
-  if (!prologue(p, s, n0)) return;
-  const FoldSmem fs = carve(lq_dyn_smem, p.W, p.C, KDA);
-  fold_tables<KDA>(p, s, n0, fs);
-  float acc[4][16];
-  reconstruct_rows<KDA>(p, s, n0, fs, acc);
-#pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-    const int i = 32 * pp + 4 * w + r;
-    float4* dst = reinterpret_cast<float4*>(p.S_out + (s * kD + i) * kD + 16 * qq);
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4)
-      dst[c4] = make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
-  }
+  const Tail tl = carve_tail(lq_dyn_smem, kTileBytes);
+  float* S = reinterpret_cast<float*>(lq_dyn_smem);
+  tile_store_rows<512>(S, tl, acc);
+  boundary_from_tile<512>(p, s, S, tl);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 
-static size_t fold_smem_bytes(const Params& p) { return fold_smem_floats(p.W, p.C, p.kda) * sizeof(float); }
+static int append_smem(const Params& p) {
+  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W - 1, true, false).end;
+}
+static int step_smem(const Params& p) {
+  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, true, true)) + kTailBytes;
+}
+static int fold_smem(const Params& p) {
+  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, false, true)) + kTailBytes;
+}
 
 template <typename K>
-static cudaError_t launch_dyn(K kernel, const Params& p, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+static cudaError_t launch(K kernel, const Params& p, int threads, int smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3((unsigned)p.n_states), dim3(kThreads), smem, st>>>(p);
+  kernel<<<dim3((unsigned)p.n_states), dim3(threads), (size_t)smem, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_init(const Params& p, cudaStream_t st) { return launch_dyn(k_init, p, fold_smem_bytes(p), st); }
+cudaError_t launch_init(const Params& p, cudaStream_t st) {
+  return launch(k_init, p, 512, kTileBytes + kTailBytes, st);
+}
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
-  if (p.kda)
-    k_append<true><<<dim3((unsigned)p.n_states), dim3(kThreads), 0, st>>>(p);
-  else
-    k_append<false><<<dim3((unsigned)p.n_states), dim3(kThreads), 0, st>>>(p);
-  return cudaGetLastError();
+  return p.kda ? launch(k_append<true>, p, 256, append_smem(p), st)
+               : launch(k_append<false>, p, 256, append_smem(p), st);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
-  return p.kda ? launch_dyn(k_step<true>, p, fold_smem_bytes(p), st)
-               : launch_dyn(k_step<false>, p, fold_smem_bytes(p), st);
+  return p.kda ? launch(k_step<true>, p, 512, step_smem(p), st) : launch(k_step<false>, p, 512, step_smem(p), st);
 }
 
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
-  return p.kda ? launch_dyn(k_fold<true>, p, fold_smem_bytes(p), st)
-               : launch_dyn(k_fold<false>, p, fold_smem_bytes(p), st);
+  return p.kda ? launch(k_fold<true>, p, 512, fold_smem(p), st) : launch(k_fold<false>, p, 512, fold_smem(p), st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {
-  return p.kda ? launch_dyn(k_export<true>, p, fold_smem_bytes(p), st)
-               : launch_dyn(k_export<false>, p, fold_smem_bytes(p), st);
+  return p.kda ? launch(k_export<true>, p, 512, fold_smem(p), st)
+               : launch(k_export<false>, p, 512, fold_smem(p), st);
 }
 
 }  // namespace lqi
