@@ -160,89 +160,85 @@ __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// staging layout: byte offsets into dynamic shared memory
+// shared-memory layouts
+
+// Blocked vector layout: block b (elements 16b..16b+15) of a 128-vector starts
+// at float 20b, so the eight lanes of a lane group, each reading its own block
+// with 16-byte loads, touch 32 distinct banks.
+constexpr int kBV = 160;
+__host__ __device__ __forceinline__ int bv(int j) { return j + ((j >> 4) << 2); }
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
+// Byte offsets into dynamic shared memory.
 struct Stage {
+  // staged by bulk copies, dense
   int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, q, k, v, alpha_cur;
-  int y, aq, zk, zq, basek, baseq, P, g, h, ec, eq, ca, bd;
+  // computed, blocked layout
+  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, line_b, lam_b, kd_b, bd_b, P_b;
+  // computed, dense
+  int basek, baseq, P, g, h, ec, eq, ca;
   int end;
 };
 
-// `slots`: record slots staged (records held, plus one for the token being
-// appended when a fold follows). `append`: stage q/k/v and the append's work
-// vectors. `fold`: room for the expanded compensators.
-__host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots, bool append,
-                                              bool fold) {
+// slots_u: staged record slots of u and alpha; slots_k: staged slots of k (the
+// fold reads every record key; the append reads keys straight into registers).
+__host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
+                                              bool append, bool fold) {
   Stage L;
   int o = 0;
-  L.codes = o;
-  o += kD * kD;
-  L.sigma = o;
-  o += 4 * kD;
-  L.lambda = o;
-  o += 4 * kD;
-  L.comp_id = o;
-  o += al16(4 * comp_id_stride);
-  L.comp_line = o;
-  o += 4 * kD * C;
-  L.rec_k = o;
-  o += 4 * kD * slots;
-  L.rec_u = o;
-  o += 4 * kD * slots;
-  L.rec_alpha = o;
-  o += kda ? 4 * kD * slots : al16(4 * ((W + 3) / 4 * 4));
-  const int va = append ? 4 * kD : 0;
-  L.q = o;
-  o += va;
-  L.k = o;
-  o += va;
-  L.v = o;
-  o += va;
-  L.alpha_cur = o;
-  o += kda ? va : 0;
-  L.y = o;
-  o += va;
-  L.aq = o;
-  o += va;
-  L.zk = o;
-  o += va;
-  L.zq = o;
-  o += va;
-  L.basek = o;
-  o += va;
-  L.baseq = o;
-  o += va;
-  L.P = o;
-  o += al16(4 * (W + 1) * (kda ? kD : 1));
-  L.g = o;
-  o += al16(4 * (W + 1));
-  L.h = o;
-  o += al16(4 * (W + 1));
-  L.ec = o;
-  o += al16(4 * (C > 0 ? C : 1));
-  L.eq = o;
-  o += al16(4 * (C > 0 ? C : 1));
-  L.ca = o;
-  o += fold ? 4 * kD * C : 0;
-  L.bd = o;
-  o += fold ? 4 * kD * C : 0;
-  L.end = al16(o);
+  auto take = [&](int bytes) {
+    const int at_ = o;
+    o += al16(bytes);
+    return at_;
+  };
+  const int va = append ? 1 : 0, fo = fold ? 1 : 0;
+  L.codes = take(kD * kD);
+  L.sigma = take(4 * kD);
+  L.lambda = take(4 * kD);
+  L.comp_id = take(4 * comp_id_stride);
+  L.comp_line = take(4 * kD * C);
+  L.rec_k = take(4 * kD * slots_k);
+  L.rec_u = take(4 * kD * slots_u);
+  L.rec_alpha = take(kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
+  L.q = take(va * 4 * kD);
+  L.k = take(va * 4 * kD);
+  L.v = take(va * 4 * kD);
+  L.alpha_cur = take(va * kda * 4 * kD);
+  L.kn_b = take(va * 4 * kBV);
+  L.qn_b = take(va * 4 * kBV);
+  L.y_b = take(va * 4 * kBV);
+  L.aq_b = take(va * 4 * kBV);
+  L.zk_b = take(va * 4 * kBV);
+  L.zq_b = take(va * 4 * kBV);
+  L.line_b = take(va * 4 * kBV * C);
+  L.lam_b = take(fo * 4 * kBV);
+  L.kd_b = take(fo * 4 * kBV * W);
+  L.bd_b = take(fo * 4 * kBV * C);
+  L.P_b = take(kda * 4 * kBV * (W + 1));
+  L.basek = take(va * 4 * kD);
+  L.baseq = take(va * 4 * kD);
+  L.P = take(4 * (W + 1));
+  L.g = take(4 * (W + 1));
+  L.h = take(4 * (W + 1));
+  L.ec = take(4 * (C > 0 ? C : 1));
+  L.eq = take(4 * (C > 0 ? C : 1));
+  L.ca = take(fo * 4 * kD * C);
+  L.end = o;
   return L;
 }
 
 // Fold workspace after region R1 = max(64 KB state tile, staging), which holds
 // the staged inputs until the reconstruction has read them and the tile after.
 struct Tail {
-  float* rowpart;  // [8][128]  per-row block partials of the squared length
+  float* rowpart;  // [128][8]  per-row block partials of the squared length
   float* colpart;  // [8][128]  per-column block partials
   float* score;    // [256]     line scores: rows 0..127, columns 128..255
-  float* gsc;      // [128]     1 / lambda
+  float* gsc_b;    // [160]     1 / lambda, blocked layout
   int* win;        // [4]
 };
 constexpr int kTileBytes = kD * kD * 4;
-constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + 128 + 4) * 4;
+constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + kBV + 4) * 4;
 
 __host__ __device__ inline int region1_bytes(const Stage& L) {
   const int r = L.end > kTileBytes ? L.end : kTileBytes;
@@ -258,8 +254,8 @@ __device__ __forceinline__ Tail carve_tail(char* base, int r1) {
   x += 8 * kD;
   t.score = x;
   x += 256;
-  t.gsc = x;
-  x += 128;
+  t.gsc_b = x;
+  x += kBV;
   t.win = reinterpret_cast<int*>(x);
   return t;
 }
@@ -277,11 +273,11 @@ namespace lqi {
 // Staging: one thread issues every copy of head-state s (n0 records held) on
 // `bar`, with the exact byte count announced first.
 __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, const Stage& L, char* sm,
-                                            uint64_t* bar, bool append) {
+                                            uint64_t* bar, bool append, bool stage_k) {
   const uint32_t rec = 4u * kD * (uint32_t)n0;
   const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
-  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + 2u * rec +
-                   alpha_bytes;
+  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec + alpha_bytes;
+  if (stage_k) bytes += rec;
   if (append) bytes += 12u * kD + (p.kda ? 4u * kD : 0u);
   mbar_expect_tx(bar, bytes);
   bulk_g2s(sm + L.codes, p.codes + s * (kD * kD), kD * kD, bar);
@@ -290,13 +286,10 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
   bulk_g2s(sm + L.comp_id, p.comp_id + s * p.comp_id_stride, 4u * (uint32_t)p.comp_id_stride, bar);
   if (p.C > 0) bulk_g2s(sm + L.comp_line, p.comp_line + s * p.C * kD, 4u * kD * (uint32_t)p.C, bar);
   if (n0 > 0) {
-    bulk_g2s(sm + L.rec_k, p.rec_k + s * p.W * kD, rec, bar);
+    if (stage_k) bulk_g2s(sm + L.rec_k, p.rec_k + s * p.W * kD, rec, bar);
     bulk_g2s(sm + L.rec_u, p.rec_u + s * p.W * kD, rec, bar);
   }
-  if (!p.kda)
-    bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
-  else if (n0 > 0)
-    bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
+  if (!p.kda || n0 > 0) bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
   if (append) {
     bulk_g2s(sm + L.q, p.q + s * kD, 4 * kD, bar);
     bulk_g2s(sm + L.k, p.k + s * kD, 4 * kD, bar);
@@ -305,21 +298,23 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
   }
 }
 
-// Decay products from staged alphas (records 1..n-1, then alpha_n = `cur`, or
-// records 1..n when cur is null). Backward running products, no division:
-//   P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.  P is [(n+1)][alen].
+// Decay products from staged alphas (records 1..n-1, then alpha_n = the current
+// token's, or records 1..n when have_cur is false). Backward running products,
+// no division: P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.
+// GDN: scalars P[m] (thread 0). KDA: blocked rows P_b[m] (threads 0..127).
 template <bool KDA>
 __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, const float* cur_vec, float cur_scalar,
-                                               bool have_cur, float* P) {
+                                               bool have_cur, float* P, float* P_b) {
   const int tid = threadIdx.x;
   if (KDA) {
     if (tid < kD) {
+      const int jb = bv(tid);
       float pr = 1.0f;
-      P[n * kD + tid] = pr;
+      P_b[n * kBV + jb] = pr;
       for (int m = n; m >= 1; --m) {
         const float am = (have_cur && m == n) ? cur_vec[tid] : rec_alpha[(m - 1) * kD + tid];
         pr = __fmul_rn(pr, am);
-        P[(m - 1) * kD + tid] = pr;
+        P_b[(m - 1) * kBV + jb] = pr;
       }
     }
   } else if (tid == 0) {
@@ -333,33 +328,62 @@ __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, co
   }
 }
 
+// P_m over the 16-element block qq of a lane: GDN broadcasts one scalar.
 template <bool KDA>
-__device__ __forceinline__ float Pj(const float* P, int m, int j) {
-  return KDA ? P[m * kD + j] : P[m];
+__device__ __forceinline__ void decay_block(const float* P, const float* P_b, int m, int qq, float d[16]) {
+  if (KDA) {
+    load16(P_b + m * kBV + 20 * qq, d);
+  } else {
+    const float x = P[m];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) d[t] = x;
+  }
+}
+
+template <bool KDA>
+__device__ __forceinline__ float decay_at(const float* P, const float* P_b, int m, int j) {
+  return KDA ? P_b[m * kBV + bv(j)] : P[m];
+}
+
+// Record keys a lane group needs for its first dot product (record grp + 1),
+// read straight from global memory into registers.
+__device__ __forceinline__ void load_record_key(const Params& p, int64_t s, int n0, float kv[16]) {
+  const int grp = threadIdx.x >> 3, qq = threadIdx.x & 7;
+  if (grp < n0) {
+    load16(p.rec_k + (s * p.W + grp) * kD + 16 * qq, kv);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) kv[t] = 0.0f;
+  }
 }
 
 // ---------------------------------------------------------------------------
-// Append (A0-A7): one token into head-state s holding n-1 records, all inputs
-// staged in shared memory. LeapQuant §3.2 (outputs from the fixed low-bit state
-// plus buffered records), App. B.2 (base term O(d_k d_v), each record
+// Append (A0-A7): one token into head-state s holding n-1 records, inputs
+// staged in shared memory (record keys of the first dot-product round in
+// registers `kv`). LeapQuant §3.2 (outputs from the fixed low-bit state plus
+// buffered records), App. B.2 (base term O(d_k d_v), each record
 // O(d_k + d_v)), App. B.3 (the smoothing scales act on the residual term only),
 // §3.3 (compensators are records at window position 0 carrying the full decay).
 // With `fold_follows`, the new record is also left in the staged buffers.
-template <bool KDA, int NT>
+// 256 threads: lane group (w, r) owns rows 32pp + 4w + r, lane qq owns the
+// 16-element block qq of every vector.
+template <bool KDA>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
-                                               float alpha_scalar, float beta, bool fold_follows) {
-  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
+                                               float alpha_scalar, float beta, bool fold_follows,
+                                               const float kv0[16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   float* P = at<float>(sm, L.P);
-  float* rk = at<float>(sm, L.rec_k);
-  float* ru = at<float>(sm, L.rec_u);
+  float* P_b = at<float>(sm, L.P_b);
   const float* kn = at<float>(sm, L.k);
   const float* qn = at<float>(sm, L.q);
-  float* y = at<float>(sm, L.y);
-  float* aq = at<float>(sm, L.aq);
-  float* zk = at<float>(sm, L.zk);
-  float* zq = at<float>(sm, L.zq);
+  float* kn_b = at<float>(sm, L.kn_b);
+  float* qn_b = at<float>(sm, L.qn_b);
+  float* y_b = at<float>(sm, L.y_b);
+  float* aq_b = at<float>(sm, L.aq_b);
+  float* zk_b = at<float>(sm, L.zk_b);
+  float* zq_b = at<float>(sm, L.zq_b);
+  float* line_b = at<float>(sm, L.line_b);
   float* basek = at<float>(sm, L.basek);
   float* baseq = at<float>(sm, L.baseq);
   float* g = at<float>(sm, L.g);
@@ -372,86 +396,94 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   const float* cl = at<float>(sm, L.comp_line);
 
   // A0: decay products over records 1..n-1 and this token's alpha.
-  decay_products<KDA>(n, at<float>(sm, L.rec_alpha), at<float>(sm, L.alpha_cur), alpha_scalar, true, P);
+  decay_products<KDA>(n, at<float>(sm, L.rec_alpha), at<float>(sm, L.alpha_cur), alpha_scalar, true, P, P_b);
   __syncthreads();
 
-  // A1: y = A_n . k_n; z = lambda . y (and the same for q, for the output).
+  // A1: y = A_n . k_n; z = lambda . y (and the same for q, for the output);
+  // blocked copies of k_n, q_n and the compensator lines for the dot products.
   if (tid < kD) {
-    const int j = tid;
-    const float A = Pj<KDA>(P, 0, j);
-    const float yy = __fmul_rn(A, kn[j]);
-    const float qa = __fmul_rn(A, qn[j]);
-    y[j] = yy;
-    aq[j] = qa;
-    zk[j] = __fmul_rn(lam[j], yy);
-    zq[j] = __fmul_rn(lam[j], qa);
+    const int j = tid, jb = bv(j);
+    const float A = decay_at<KDA>(P, P_b, 0, j);
+    const float kj = kn[j], qj = qn[j];
+    const float yy = __fmul_rn(A, kj);
+    const float qa = __fmul_rn(A, qj);
+    kn_b[jb] = kj;
+    qn_b[jb] = qj;
+    y_b[jb] = yy;
+    aq_b[jb] = qa;
+    zk_b[jb] = __fmul_rn(lam[j], yy);
+    zq_b[jb] = __fmul_rn(lam[j], qa);
+  } else {
+    const int j = tid - kD, jb = bv(j);
+    for (int c = 0; c < p.C; ++c) line_b[c * kBV + jb] = cl[c * kD + j];
   }
   __syncthreads();
 
-  // A2: fused dequantize + two matvecs. Lane group (w, r) owns rows
-  // pp * 4 * NW + 4w + r; lane qq owns the 16-code block 16qq..16qq+15 of each
-  // row: one 16-byte load, 16 exact conversions, 2 fmas per code, the tree.
-  {
-    float zkr[16], zqr[16];
-    load16(zk + 16 * qq, zkr);
-    load16(zq + 16 * qq, zqr);
-    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
-#pragma unroll
-    for (int pp = 0; pp < RPT; ++pp) {
-      const int i = pp * 4 * NW + 4 * w + r;
-      float f[16];
-      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
-      float ak = 0.0f, aqq = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        ak = __fmaf_rn(f[t], zkr[t], ak);
-        aqq = __fmaf_rn(f[t], zqr[t], aqq);
-      }
-      ak = tree8(ak);
-      aqq = tree8(aqq);
-      if (qq == 0) {
-        basek[i] = __fmul_rn(sg[i], ak);
-        baseq[i] = __fmul_rn(sg[i], aqq);
-      }
-    }
-  }
-
-  // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
+  // A3/A4 reads (before the matvec, so that the record keys held in registers
+  // are consumed early), one lane group per dot product: records m = 1..n-1, then the
   // compensators, then k_n . q_n (the new record's output term, P_n = 1).
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
     const int njobs = nrec + p.C + 1;
-    for (int base = 0; base < njobs; base += NT / 8) {
+    for (int base = 0; base < njobs; base += 32) {
       const int job = base + grp;
       float pa = 0.0f, pb = 0.0f;
       if (job < njobs) {
         if (job < nrec) {
           const int m = job + 1;
-          float kv[16], kx[16], qx[16];
-          load16(rk + (m - 1) * kD + 16 * qq, kv);
-          load16(kn + 16 * qq, kx);
-          load16(qn + 16 * qq, qx);
+          float kv[16];
+          if (base == 0) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float Pm = Pj<KDA>(P, m, 16 * qq + t);
-            pa = __fmaf_rn(kv[t], __fmul_rn(Pm, kx[t]), pa);
-            pb = __fmaf_rn(kv[t], __fmul_rn(Pm, qx[t]), pb);
+            for (int t = 0; t < 16; ++t) kv[t] = kv0[t];
+          } else {
+            load16(p.rec_k + (s * p.W + (m - 1)) * kD + 16 * qq, kv);
+          }
+          const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
+          const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
+          const float4* pm4 = reinterpret_cast<const float4*>(P_b + m * kBV + 20 * qq);
+          const float pms = KDA ? 0.0f : P[m];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 kx = kx4[c4], qx = qx4[c4];
+            const float4 pm = KDA ? pm4[c4] : make_float4(pms, pms, pms, pms);
+            const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pa = __fmaf_rn(kv[4 * c4 + e], __fmul_rn(pmv[e], kxs[e]), pa);
+              pb = __fmaf_rn(kv[4 * c4 + e], __fmul_rn(pmv[e], qxs[e]), pb);
+            }
           }
         } else if (job < nrec + p.C) {
           const int c = job - nrec;
           const int id = cid[c];
-          const float* line = cl + c * kD;
+          const float4* b4 = reinterpret_cast<const float4*>(line_b + c * kBV + 20 * qq);
+          const float4* y4 = reinterpret_cast<const float4*>(y_b + 20 * qq);
+          const float4* a4 = reinterpret_cast<const float4*>(aq_b + 20 * qq);
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int j = 16 * qq + t;
-            const float b = (id < kD) ? line[j] : (j == id - kD ? 1.0f : 0.0f);
-            pa = __fmaf_rn(b, y[j], pa);
-            pb = __fmaf_rn(b, aq[j], pb);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 bb = b4[c4], yv = y4[c4], av = a4[c4];
+            float bs[4] = {bb.x, bb.y, bb.z, bb.w};
+            const float ys[4] = {yv.x, yv.y, yv.z, yv.w}, as[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
+              pa = __fmaf_rn(bs[e], ys[e], pa);
+              pb = __fmaf_rn(bs[e], as[e], pb);
+            }
           }
         } else {
+          const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
+          const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
 #pragma unroll
-          for (int t = 0; t < 16; ++t) pb = __fmaf_rn(kn[16 * qq + t], qn[16 * qq + t], pb);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 kx = kx4[c4], qx = qx4[c4];
+            pb = __fmaf_rn(kx.x, qx.x, pb);
+            pb = __fmaf_rn(kx.y, qx.y, pb);
+            pb = __fmaf_rn(kx.z, qx.z, pb);
+            pb = __fmaf_rn(kx.w, qx.w, pb);
+          }
         }
       }
       pa = tree8(pa);
@@ -469,10 +501,39 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       }
     }
   }
+
+  // A2: fused dequantize + two matvecs: one 16-byte code load, 16 exact
+  // conversions and 2 fmas per code, then the tree.
+  {
+    float zkr[16], zqr[16];
+    load16(zk_b + 20 * qq, zkr);
+    load16(zq_b + 20 * qq, zqr);
+    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
+      float f[16];
+      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
+      float ak = 0.0f, aqq = 0.0f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        ak = __fmaf_rn(f[t], zkr[t], ak);
+        aqq = __fmaf_rn(f[t], zqr[t], aqq);
+      }
+      ak = tree8(ak);
+      aqq = tree8(aqq);
+      if (qq == 0) {
+        basek[i] = __fmul_rn(sg[i], ak);
+        baseq[i] = __fmul_rn(sg[i], aqq);
+      }
+    }
+  }
+
   __syncthreads();
 
   // A3-A5 per value row: acc = base; compensators in order; records in order;
   // u_n = beta (v - acc). A6: the output in any order. A7: store record n.
+  float* ru = at<float>(sm, L.rec_u);
   const float* vv = at<float>(sm, L.v);
   if (tid < kD) {
     const int i = tid;
@@ -494,10 +555,10 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     p.rec_u[(s * p.W + (n - 1)) * kD + i] = u;
     p.o[s * kD + i] = oo;
     if (fold_follows) ru[(n - 1) * kD + i] = u;
-  } else if (tid < 2 * kD) {
+  } else {
     const int j = tid - kD;
     p.rec_k[(s * p.W + (n - 1)) * kD + j] = kn[j];
-    if (fold_follows) rk[(n - 1) * kD + j] = kn[j];
+    if (fold_follows) at<float>(sm, L.rec_k)[(n - 1) * kD + j] = kn[j];
     if (KDA)
       p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + j] = at<float>(sm, L.alpha_cur)[j];
     else if (j == 0)
@@ -514,103 +575,116 @@ namespace lqi {
 // coordinates at the window boundary; §3.3: compensators are the largest
 // outlier lines kept in fp32; §3.4: per-key-channel smoothing scales
 // sqrt(mean |.|) with a floor; then one rounding to int8 per row step.
+// 256 threads; a thread owns rows 32pp + 4w + r (pp = 0..3), columns 16qq..16qq+15.
 
-// F0: record keys scaled by their decay products, in place over the staged keys
-// (kd_m = P_m . k_m), and the expanded compensators (a_c, P_0 . b_c).
-template <bool KDA, int NT>
+// F0: record keys scaled by their decay products (kd_m = P_m . k_m), the
+// expanded compensators (a_c, P_0 . b_c) and lambda, blocked where lanes read
+// them block-wise.
+template <bool KDA>
 __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage& L, char* sm) {
   const int tid = threadIdx.x;
   const float* P = at<float>(sm, L.P);
-  float* rk = at<float>(sm, L.rec_k);
-  for (int e = tid; e < n * kD; e += NT) {
+  const float* P_b = at<float>(sm, L.P_b);
+  const float* rk = at<float>(sm, L.rec_k);
+  float* kd_b = at<float>(sm, L.kd_b);
+  for (int e = tid; e < n * kD; e += 256) {
     const int m1 = e >> 7, j = e & (kD - 1);
-    rk[e] = __fmul_rn(Pj<KDA>(P, m1 + 1, j), rk[e]);
+    kd_b[m1 * kBV + bv(j)] = __fmul_rn(decay_at<KDA>(P, P_b, m1 + 1, j), rk[e]);
   }
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
   float* ca = at<float>(sm, L.ca);
-  float* bd = at<float>(sm, L.bd);
-  for (int e = tid; e < p.C * kD; e += NT) {
+  float* bd_b = at<float>(sm, L.bd_b);
+  for (int e = tid; e < p.C * kD; e += 256) {
     const int c = e >> 7, x = e & (kD - 1);
     const int id = cid[c];
-    const float lv = cl[c * kD + x];
+    const float lv = cl[e];
     const float a = (id < kD) ? (x == id ? 1.0f : 0.0f) : lv;
     const float b = (id < kD) ? lv : (x == id - kD ? 1.0f : 0.0f);
     ca[e] = a;
-    bd[e] = __fmul_rn(Pj<KDA>(P, 0, x), b);
+    bd_b[c * kBV + bv(x)] = __fmul_rn(decay_at<KDA>(P, P_b, 0, x), b);
   }
+  if (tid < kD) at<float>(sm, L.lam_b)[bv(tid)] = at<float>(sm, L.lambda)[tid];
   __syncthreads();
 }
 
-// F1 for the RPT rows x 16 columns a thread owns (rows pp*4*NW + 4w + r,
-// columns 16qq..16qq+15): S_ij = ((sigma_i Cd_ij) lambda_j) P_0[j], then the
-// compensators in order, then the records in order, each an fma.
-template <bool KDA, int NT>
-__device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm,
-                                                 float acc[][16]) {
-  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
+// F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
+// lambda_j) P_0[j], then the compensators in order, then the records in order,
+// each an fma.
+template <bool KDA>
+__device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   const float* P = at<float>(sm, L.P);
+  const float* P_b = at<float>(sm, L.P_b);
   const float* sg = at<float>(sm, L.sigma);
   const float* ca = at<float>(sm, L.ca);
-  const float* bd = at<float>(sm, L.bd);
-  const float* kd = at<float>(sm, L.rec_k);
+  const float* bd_b = at<float>(sm, L.bd_b);
+  const float* kd_b = at<float>(sm, L.kd_b);
   const float* U = at<float>(sm, L.rec_u);
-  float lam[16], p0[16];
-  load16(at<float>(sm, L.lambda) + 16 * qq, lam);
-  if (KDA) {
-    load16(P + 16 * qq, p0);
-  } else {
+  {
+    float lam[16], p0[16];
+    load16(at<float>(sm, L.lam_b) + 20 * qq, lam);
+    decay_block<KDA>(P, P_b, 0, qq, p0);
+    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) p0[t] = P[0];
-  }
-  const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
+      const float s_i = sg[i];
+      float f[16];
+      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
 #pragma unroll
-  for (int pp = 0; pp < RPT; ++pp) {
-    const int i = pp * 4 * NW + 4 * w + r;
-    const float s_i = sg[i];
-    float f[16];
-    codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
-#pragma unroll
-    for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[t]), lam[t]), p0[t]);
+      for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[t]), lam[t]), p0[t]);
+    }
   }
   for (int c = 0; c < p.C; ++c) {
-    float b[16];
-    load16(bd + c * kD + 16 * qq, b);
+    float a[4];
 #pragma unroll
-    for (int pp = 0; pp < RPT; ++pp) {
-      const float a = ca[c * kD + pp * 4 * NW + 4 * w + r];
+    for (int pp = 0; pp < 4; ++pp) a[pp] = ca[c * kD + 32 * pp + 4 * w + r];
+    const float4* b4 = reinterpret_cast<const float4*>(bd_b + c * kBV + 20 * qq);
 #pragma unroll
-      for (int t = 0; t < 16; ++t) acc[pp][t] = __fmaf_rn(a, b[t], acc[pp][t]);
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 b = b4[c4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        acc[pp][4 * c4 + 0] = __fmaf_rn(a[pp], b.x, acc[pp][4 * c4 + 0]);
+        acc[pp][4 * c4 + 1] = __fmaf_rn(a[pp], b.y, acc[pp][4 * c4 + 1]);
+        acc[pp][4 * c4 + 2] = __fmaf_rn(a[pp], b.z, acc[pp][4 * c4 + 2]);
+        acc[pp][4 * c4 + 3] = __fmaf_rn(a[pp], b.w, acc[pp][4 * c4 + 3]);
+      }
     }
   }
   for (int m = 0; m < n; ++m) {
-    float kdv[16];
-    load16(kd + m * kD + 16 * qq, kdv);
+    float u[4];
 #pragma unroll
-    for (int pp = 0; pp < RPT; ++pp) {
-      const float u = U[m * kD + pp * 4 * NW + 4 * w + r];
+    for (int pp = 0; pp < 4; ++pp) u[pp] = U[m * kD + 32 * pp + 4 * w + r];
+    const float4* k4 = reinterpret_cast<const float4*>(kd_b + m * kBV + 20 * qq);
 #pragma unroll
-      for (int t = 0; t < 16; ++t) acc[pp][t] = __fmaf_rn(u, kdv[t], acc[pp][t]);
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 b = k4[c4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        acc[pp][4 * c4 + 0] = __fmaf_rn(u[pp], b.x, acc[pp][4 * c4 + 0]);
+        acc[pp][4 * c4 + 1] = __fmaf_rn(u[pp], b.y, acc[pp][4 * c4 + 1]);
+        acc[pp][4 * c4 + 2] = __fmaf_rn(u[pp], b.z, acc[pp][4 * c4 + 2]);
+        acc[pp][4 * c4 + 3] = __fmaf_rn(u[pp], b.w, acc[pp][4 * c4 + 3]);
+      }
     }
   }
 }
 
-// Store a thread's rows into the swizzled tile S and record their row
-// partials and row scores (squared lengths).
-template <int NT>
-__device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float acc[][16]) {
-  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
+// Store a thread's rows into the swizzled tile S; record their row partials
+// ([row][block]) and row scores (squared lengths).
+__device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 #pragma unroll
-  for (int pp = 0; pp < RPT; ++pp) {
-    const int i = pp * 4 * NW + 4 * w + r;
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
     float pr = 0.0f;
 #pragma unroll
     for (int t = 0; t < 16; ++t) pr = __fmaf_rn(acc[pp][t], acc[pp][t], pr);
-    tl.rowpart[qq * kD + i] = pr;
+    tl.rowpart[i * 8 + qq] = pr;
     const float rho = tree8(pr);
     if (qq == 0) tl.score[i] = rho;
 #pragma unroll
@@ -621,49 +695,54 @@ __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float 
   __syncthreads();
 }
 
+// Column block chain: fma (squares) or add (absolute values) over rows
+// 16b..16b+15 of column j, ascending.
+template <bool SQUARES>
+__device__ __forceinline__ float column_block(const float* S, int b, int j) {
+  float x[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
+  float acc = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) acc = SQUARES ? __fmaf_rn(x[t], x[t], acc) : __fadd_rn(acc, fabsf(x[t]));
+  return acc;
+}
+
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
-template <int NT>
 __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
-  constexpr int NW = NT / 32, RPT = 128 / (4 * NW);
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 
-  // Column scores: block partial b of column j is an fma chain over rows 16b..16b+15.
+  // Column scores.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += NT / kD) {
-      float x[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
-      float pc = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) pc = __fmaf_rn(x[t], x[t], pc);
-      tl.colpart[b * kD + j] = pc;
-    }
+    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<true>(S, b, j);
   }
   __syncthreads();
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
 
-  // F2: C greedy rounds of the longest line, ties to the smallest id.
+  // F2: C greedy rounds of the longest line, ties to the smallest id. Lane L
+  // scans ids L, L+32, ... in ascending order, then the warp keeps the larger
+  // score (the smaller id on a tie).
   for (int c = 0; c < p.C; ++c) {
     if (tid < 32) {
-      float bv = tl.score[8 * tid];
-      int bi = 8 * tid;
+      float bv_ = tl.score[tid];
+      int bi = tid;
 #pragma unroll
       for (int e = 1; e < 8; ++e) {
-        const float v = tl.score[8 * tid + e];
-        if (v > bv) {
-          bv = v;
-          bi = 8 * tid + e;
+        const float v = tl.score[tid + 32 * e];
+        if (v > bv_) {
+          bv_ = v;
+          bi = tid + 32 * e;
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_down_sync(0xffffffffu, bv, off);
+        const float ov = __shfl_down_sync(0xffffffffu, bv_, off);
         const int oi = __shfl_down_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
+        if (ov > bv_ || (ov == bv_ && oi < bi)) {
+          bv_ = ov;
           bi = oi;
         }
       }
@@ -683,16 +762,10 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         line[j] = *e;
         *e = 0.0f;
         const int b = win >> 4;
-        float x[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
-        float pc = 0.0f;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) pc = __fmaf_rn(x[t], x[t], pc);
-        tl.colpart[b * kD + j] = pc;
+        tl.colpart[b * kD + j] = column_block<true>(S, b, j);
         tl.score[kD + j] = tree8_mem(tl.colpart + j, kD);
       } else if (tid < kD + 8) {
-        tl.rowpart[(tid - kD) * kD + win] = 0.0f;
+        tl.rowpart[win * 8 + (tid - kD)] = 0.0f;
       } else if (tid == kD + 8) {
         tl.score[win] = 0.0f;
       }
@@ -711,8 +784,8 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         float pr = 0.0f;
 #pragma unroll
         for (int t = 0; t < 16; ++t) pr = __fmaf_rn(x[t], x[t], pr);
-        tl.rowpart[q * kD + i] = pr;
-        tl.score[i] = tree8_mem(tl.rowpart + i, kD);
+        tl.rowpart[i * 8 + q] = pr;
+        tl.score[i] = tree8_mem(tl.rowpart + i * 8, 1);
       } else if (tid < kD + 8) {
         tl.colpart[(tid - kD) * kD + js] = 0.0f;
       } else if (tid == kD + 8) {
@@ -725,33 +798,25 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   // F3: smoothing scales from the residual's column sums of |R|.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += NT / kD) {
-      float x[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
-      float pa = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) pa = __fadd_rn(pa, fabsf(x[t]));
-      tl.colpart[b * kD + j] = pa;
-    }
+    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<false>(S, b, j);
   }
   __syncthreads();
   if (tid < kD) {
     const float mu = __fmul_rn(tree8_mem(tl.colpart + tid, kD), 1.0f / (float)kD);
     const float lam = p.smooth ? fmaxf(__fsqrt_rn(mu), p.lambda_floor) : 1.0f;
     p.lambda[s * kD + tid] = lam;
-    tl.gsc[tid] = __fdiv_rn(1.0f, lam);
+    tl.gsc_b[bv(tid)] = __fdiv_rn(1.0f, lam);
   }
   __syncthreads();
 
   // F4-F5: per-row absmax of t = R / lambda, one reciprocal per row, round once.
   {
     float g[16];
-    load16(tl.gsc + 16 * qq, g);
+    load16(tl.gsc_b + 20 * qq, g);
     int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
 #pragma unroll
-    for (int pp = 0; pp < RPT; ++pp) {
-      const int i = pp * 4 * NW + 4 * w + r;
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
       float t[16];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -793,50 +858,55 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
 namespace lqi {
 
 // ---------------------------------------------------------------------------
-// kernels: one CTA per head-state
+// kernels: one CTA of 256 threads per head-state
 
 extern __shared__ __align__(128) char lq_dyn_smem[];
 
 // Thread 0 starts the copies (at once when `known_n0` >= 0, else after reading
-// the record count); every thread reads the header and count meanwhile. Then
-// every thread waits, boundedly, for the copies. Returns the record count held
-// (>= 0) or -1 after recording an error; the result is uniform over the CTA.
-__device__ __forceinline__ int stage_and_check(const Params& p, int64_t s, int known_n0, const Stage& L,
-                                               uint64_t* bar, int* s_issued, bool append, int max_n0) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
+// the record count) and publishes the count it used in *s_issued; every thread
+// reads the header and the count meanwhile. Returns after the __syncthreads
+// that publishes *s_issued.
+__device__ __forceinline__ void stage_start(const Params& p, int64_t s, int known_n0, const Stage& L, uint64_t* bar,
+                                            int* s_issued, bool append, bool stage_k, int max_n0, bool& hdr,
+                                            int& cnt) {
+  if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     int n0 = known_n0;
     if (n0 < 0) {
       const int c = p.counts[s];
       n0 = (c >= 0 && c <= max_n0) ? c : -1;
     }
-    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append);
+    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append, stage_k);
     *s_issued = n0;
   }
-  const bool hdr = header_ok(p);
-  const int cnt = p.counts[s];
+  hdr = header_ok(p);
+  cnt = p.counts[s];
   __syncthreads();
-  const int n0 = *s_issued;
+}
+
+// Bounded wait for the copies, then the checks. Returns the record count held
+// (>= 0) or -1 after recording an error; uniform over the CTA.
+__device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t* bar, int n0, bool hdr, int cnt,
+                                            bool append) {
   if (n0 >= 0) {
-    bool ok = mbar_wait_bounded(bar, 0);
+    const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
       if (!ok) (void)mbar_wait_bounded(bar, 0);  // one more bounded chance for copies in flight
-      if (tid == 0) set_error(p, LQ_ERR_TIMEOUT, s);
+      if (threadIdx.x == 0) set_error(p, LQ_ERR_TIMEOUT, s);
       return -1;
     }
   }
   int err = 0;
   if (!hdr || cnt < 0 || cnt > p.W)
     err = LQ_ERR_STATE;
-  else if (p.phase >= 0 && append && cnt != p.phase)
+  else if (append && p.phase >= 0 && cnt != p.phase)
     err = LQ_ERR_PHASE;
   else if (append && cnt >= p.W)
     err = LQ_ERR_WINDOW_FULL;
   else if (cnt != n0)
     err = LQ_ERR_STATE;
   if (err) {
-    if (tid == 0) set_error(p, err, s);
+    if (threadIdx.x == 0) set_error(p, err, s);
     return -1;
   }
   return cnt;
@@ -844,89 +914,111 @@ __device__ __forceinline__ int stage_and_check(const Params& p, int64_t s, int k
 
 // Append only (no fold): the W-1 decode steps that cannot fill the window, and lq_append.
 template <bool KDA>
-__global__ void __launch_bounds__(256, 5) k_append(Params p) {
+__global__ void __launch_bounds__(256, 4) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W - 1, true, false);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W - 1, 0, true, false);
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  const int n0 = stage_and_check(p, s, known, L, &bar, &s_issued, true, p.W - 1);
+  float kv[16];
+  if (known >= 0) load_record_key(p, s, known, kv);
+  bool hdr;
+  int cnt;
+  stage_start(p, s, known, L, &bar, &s_issued, true, false, p.W - 1, hdr, cnt);
+  const int issued = s_issued;
+  if (known < 0) load_record_key(p, s, issued, kv);
+  const int n0 = stage_finish(p, s, &bar, issued, hdr, cnt, true);
   if (n0 < 0) return;
-  append_compute<KDA, 256>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
+  append_compute<KDA>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false, kv);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
 template <bool KDA>
-__global__ void __launch_bounds__(512, 2) k_step(Params p) {
+__global__ void __launch_bounds__(256, 2) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, true, true);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, true, true);
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  const int n0 = stage_and_check(p, s, known, L, &bar, &s_issued, true, p.W - 1);
+  float kv[16];
+  if (known >= 0) load_record_key(p, s, known, kv);
+  bool hdr;
+  int cnt;
+  stage_start(p, s, known, L, &bar, &s_issued, true, true, p.W - 1, hdr, cnt);
+  const int issued = s_issued;
+  if (known < 0) load_record_key(p, s, issued, kv);
+  const int n0 = stage_finish(p, s, &bar, issued, hdr, cnt, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
-  append_compute<KDA, 512>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
+  append_compute<KDA>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W, kv);
   if (n < p.W) {
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
   __syncthreads();
-  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
-  float acc[2][16];
-  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+  fold_tables<KDA>(p, n, L, lq_dyn_smem);
+  float acc[4][16];
+  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
   const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows<512>(S, tl, acc);
-  boundary_from_tile<512>(p, s, S, tl);
+  tile_store_rows(S, tl, acc);
+  boundary_from_tile(p, s, S, tl);
 }
 
 // Fold with the records held (any count 0..W): lq_fold.
 template <bool KDA>
-__global__ void __launch_bounds__(512, 2) k_fold(Params p) {
+__global__ void __launch_bounds__(256, 2) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, false, true);
-  const int n = stage_and_check(p, s, -1, L, &bar, &s_issued, false, p.W);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, false, true);
+  bool hdr;
+  int cnt;
+  stage_start(p, s, -1, L, &bar, &s_issued, false, true, p.W, hdr, cnt);
+  const int n = stage_finish(p, s, &bar, s_issued, hdr, cnt, false);
   if (n < 0) return;
-  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P));
+  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
+                      at<float>(lq_dyn_smem, L.P_b));
   __syncthreads();
-  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
-  float acc[2][16];
-  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+  fold_tables<KDA>(p, n, L, lq_dyn_smem);
+  float acc[4][16];
+  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();
   const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows<512>(S, tl, acc);
-  boundary_from_tile<512>(p, s, S, tl);
+  tile_store_rows(S, tl, acc);
+  boundary_from_tile(p, s, S, tl);
 }
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
 template <bool KDA>
-__global__ void __launch_bounds__(512, 2) k_export(Params p) {
+__global__ void __launch_bounds__(256, 2) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_issued;
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, false, true);
-  const int n = stage_and_check(p, s, -1, L, &bar, &s_issued, false, p.W);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, false, true);
+  bool hdr;
+  int cnt;
+  stage_start(p, s, -1, L, &bar, &s_issued, false, true, p.W, hdr, cnt);
+  const int n = stage_finish(p, s, &bar, s_issued, hdr, cnt, false);
   if (n < 0) return;
-  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P));
+  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
+                      at<float>(lq_dyn_smem, L.P_b));
   __syncthreads();
-  fold_tables<KDA, 512>(p, n, L, lq_dyn_smem);
-  float acc[2][16];
-  reconstruct_rows<KDA, 512>(p, n, L, lq_dyn_smem, acc);
+  fold_tables<KDA>(p, n, L, lq_dyn_smem);
+  float acc[4][16];
+  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
 #pragma unroll
-  for (int pp = 0; pp < 2; ++pp) {
-    const int i = pp * 64 + 4 * w + r;
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
     float4* dst = reinterpret_cast<float4*>(p.S_out + (s * kD + i) * kD + 16 * qq);
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4)
@@ -935,7 +1027,7 @@ __global__ void __launch_bounds__(512, 2) k_export(Params p) {
 }
 
 // Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
-__global__ void __launch_bounds__(512, 2) k_init(Params p) {
+__global__ void __launch_bounds__(256, 2) k_init(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -948,10 +1040,10 @@ __global__ void __launch_bounds__(512, 2) k_init(Params p) {
     p.hdr->reserved0 = 0;
     p.hdr->bad_state = -1;
   }
-  float acc[2][16];
+  float acc[4][16];
 #pragma unroll
-  for (int pp = 0; pp < 2; ++pp) {
-    const int i = pp * 64 + 4 * w + r;
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
     if (p.S0) {
       load16(p.S0 + (s * kD + i) * kD + 16 * qq, acc[pp]);
     } else {
@@ -961,51 +1053,47 @@ __global__ void __launch_bounds__(512, 2) k_init(Params p) {
   }
   const Tail tl = carve_tail(lq_dyn_smem, kTileBytes);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows<512>(S, tl, acc);
-  boundary_from_tile<512>(p, s, S, tl);
+  tile_store_rows(S, tl, acc);
+  boundary_from_tile(p, s, S, tl);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 
 static int append_smem(const Params& p) {
-  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W - 1, true, false).end;
+  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W - 1, 0, true, false).end;
 }
 static int step_smem(const Params& p) {
-  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, true, true)) + kTailBytes;
+  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, p.W, true, true)) + kTailBytes;
 }
 static int fold_smem(const Params& p) {
-  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, false, true)) + kTailBytes;
+  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, p.W, false, true)) + kTailBytes;
 }
 
 template <typename K>
-static cudaError_t launch(K kernel, const Params& p, int threads, int smem, cudaStream_t st) {
+static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3((unsigned)p.n_states), dim3(threads), (size_t)smem, st>>>(p);
+  kernel<<<dim3((unsigned)p.n_states), dim3(256), (size_t)smem, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_init(const Params& p, cudaStream_t st) {
-  return launch(k_init, p, 512, kTileBytes + kTailBytes, st);
-}
+cudaError_t launch_init(const Params& p, cudaStream_t st) { return launch(k_init, p, kTileBytes + kTailBytes, st); }
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_append<true>, p, 256, append_smem(p), st)
-               : launch(k_append<false>, p, 256, append_smem(p), st);
+  return p.kda ? launch(k_append<true>, p, append_smem(p), st) : launch(k_append<false>, p, append_smem(p), st);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_step<true>, p, 512, step_smem(p), st) : launch(k_step<false>, p, 512, step_smem(p), st);
+  return p.kda ? launch(k_step<true>, p, step_smem(p), st) : launch(k_step<false>, p, step_smem(p), st);
 }
 
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_fold<true>, p, 512, fold_smem(p), st) : launch(k_fold<false>, p, 512, fold_smem(p), st);
+  return p.kda ? launch(k_fold<true>, p, fold_smem(p), st) : launch(k_fold<false>, p, fold_smem(p), st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_export<true>, p, 512, fold_smem(p), st)
-               : launch(k_export<false>, p, 512, fold_smem(p), st);
+  return p.kda ? launch(k_export<true>, p, fold_smem(p), st) : launch(k_export<false>, p, fold_smem(p), st);
 }
 
 }  // namespace lqi
