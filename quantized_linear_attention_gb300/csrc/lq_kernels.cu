@@ -320,6 +320,7 @@ __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, co
   } else if (tid == 0) {
     float pr = 1.0f;
     P[n] = pr;
+#pragma unroll 8
     for (int m = n; m >= 1; --m) {
       const float am = (have_cur && m == n) ? cur_scalar : rec_alpha[m - 1];
       pr = __fmul_rn(pr, am);
@@ -345,22 +346,9 @@ __device__ __forceinline__ float decay_at(const float* P, const float* P_b, int 
   return KDA ? P_b[m * kBV + bv(j)] : P[m];
 }
 
-// Record keys a lane group needs for its first dot product (record grp + 1),
-// read straight from global memory into registers.
-__device__ __forceinline__ void load_record_key(const Params& p, int64_t s, int n0, float kv[16]) {
-  const int grp = threadIdx.x >> 3, qq = threadIdx.x & 7;
-  if (grp < n0) {
-    load16(p.rec_k + (s * p.W + grp) * kD + 16 * qq, kv);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) kv[t] = 0.0f;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Append (A0-A7): one token into head-state s holding n-1 records, inputs
-// staged in shared memory (record keys of the first dot-product round in
-// registers `kv`). LeapQuant §3.2 (outputs from the fixed low-bit state plus
+// staged in shared memory. LeapQuant §3.2 (outputs from the fixed low-bit state plus
 // buffered records), App. B.2 (base term O(d_k d_v), each record
 // O(d_k + d_v)), App. B.3 (the smoothing scales act on the residual term only),
 // §3.3 (compensators are records at window position 0 carrying the full decay).
@@ -369,8 +357,7 @@ __device__ __forceinline__ void load_record_key(const Params& p, int64_t s, int 
 // 16-element block qq of every vector.
 template <bool KDA>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
-                                               float alpha_scalar, float beta, bool fold_follows,
-                                               const float kv0[16]) {
+                                               float alpha_scalar, float beta, bool fold_follows) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   float* P = at<float>(sm, L.P);
@@ -419,8 +406,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   }
   __syncthreads();
 
-  // A3/A4 reads (before the matvec, so that the record keys held in registers
-  // are consumed early), one lane group per dot product: records m = 1..n-1, then the
+  // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
   // compensators, then k_n . q_n (the new record's output term, P_n = 1).
   {
     const int grp = tid >> 3;
@@ -432,27 +418,22 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       if (job < njobs) {
         if (job < nrec) {
           const int m = job + 1;
-          float kv[16];
-          if (base == 0) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) kv[t] = kv0[t];
-          } else {
-            load16(p.rec_k + (s * p.W + (m - 1)) * kD + 16 * qq, kv);
-          }
+          const float4* kv4 = reinterpret_cast<const float4*>(at<float>(sm, L.rec_k) + (m - 1) * kD + 16 * qq);
           const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
           const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
           const float4* pm4 = reinterpret_cast<const float4*>(P_b + m * kBV + 20 * qq);
           const float pms = KDA ? 0.0f : P[m];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 kx = kx4[c4], qx = qx4[c4];
+            const float4 kvc = kv4[c4], kx = kx4[c4], qx = qx4[c4];
             const float4 pm = KDA ? pm4[c4] : make_float4(pms, pms, pms, pms);
+            const float kvs[4] = {kvc.x, kvc.y, kvc.z, kvc.w};
             const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
             const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              pa = __fmaf_rn(kv[4 * c4 + e], __fmul_rn(pmv[e], kxs[e]), pa);
-              pb = __fmaf_rn(kv[4 * c4 + e], __fmul_rn(pmv[e], qxs[e]), pb);
+              pa = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], kxs[e]), pa);
+              pb = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], qxs[e]), pb);
             }
           }
         } else if (job < nrec + p.C) {
@@ -502,33 +483,49 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     }
   }
 
-  // A2: fused dequantize + two matvecs: one 16-byte code load, 16 exact
-  // conversions and 2 fmas per code, then the tree.
+  // A2: fused dequantize + two matvecs: one 16-byte code load per row, exact
+  // conversions and 2 fmas per code. The z blocks are consumed 4 elements at a
+  // time with the thread's 4 rows interleaved; each row's chain still runs over
+  // its 16 elements in ascending order, then the tree.
   {
-    float zkr[16], zqr[16];
-    load16(zk_b + 20 * qq, zkr);
-    load16(zq_b + 20 * qq, zqr);
     const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
+    uint32_t cw[4][4];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int4 c = *reinterpret_cast<const int4*>(cb + (32 * pp + 4 * w + r) * kD);
+      cw[pp][0] = (uint32_t)c.x ^ 0x80808080u;
+      cw[pp][1] = (uint32_t)c.y ^ 0x80808080u;
+      cw[pp][2] = (uint32_t)c.z ^ 0x80808080u;
+      cw[pp][3] = (uint32_t)c.w ^ 0x80808080u;
+    }
+    float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
+    const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 a = zk4[c4], b = zq4[c4];
+      const float za[4] = {a.x, a.y, a.z, a.w}, zb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float f = code_f(cw[pp][c4], e);
+          ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
+          aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
+        }
+      }
+    }
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
-      float f[16];
-      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
-      float ak = 0.0f, aqq = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        ak = __fmaf_rn(f[t], zkr[t], ak);
-        aqq = __fmaf_rn(f[t], zqr[t], aqq);
-      }
-      ak = tree8(ak);
-      aqq = tree8(aqq);
+      const float sk = tree8(ak[pp]);
+      const float sq = tree8(aqq[pp]);
       if (qq == 0) {
-        basek[i] = __fmul_rn(sg[i], ak);
-        baseq[i] = __fmul_rn(sg[i], aqq);
+        basek[i] = __fmul_rn(sg[i], sk);
+        baseq[i] = __fmul_rn(sg[i], sq);
       }
     }
   }
-
   __syncthreads();
 
   // A3-A5 per value row: acc = base; compensators in order; records in order;
@@ -545,6 +542,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       acc = __fmaf_rn(a, ec[c], acc);
       oo = __fmaf_rn(a, eq[c], oo);
     }
+#pragma unroll 4
     for (int m = 1; m <= n - 1; ++m) {
       const float um = ru[(m - 1) * kD + i];
       acc = __fmaf_rn(um, g[m], acc);
@@ -912,26 +910,26 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
   return cnt;
 }
 
-// Append only (no fold): the W-1 decode steps that cannot fill the window, and lq_append.
+// Append only (no fold): the W-1 decode steps that cannot fill the window, and
+// lq_append. With a stated phase the staging area holds exactly `phase` records.
+__host__ __device__ inline int append_slots(int W, int phase) { return (phase >= 0 && phase < W) ? phase : W - 1; }
+
 template <bool KDA>
-__global__ void __launch_bounds__(256, 4) k_append(Params p) {
+__global__ void __launch_bounds__(256, 6) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_issued;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W - 1, 0, true, false);
+  const int slots = append_slots(p.W, p.phase);
+  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, slots, slots, true, false);
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  float kv[16];
-  if (known >= 0) load_record_key(p, s, known, kv);
   bool hdr;
   int cnt;
-  stage_start(p, s, known, L, &bar, &s_issued, true, false, p.W - 1, hdr, cnt);
-  const int issued = s_issued;
-  if (known < 0) load_record_key(p, s, issued, kv);
-  const int n0 = stage_finish(p, s, &bar, issued, hdr, cnt, true);
+  stage_start(p, s, known, L, &bar, &s_issued, true, true, slots, hdr, cnt);
+  const int n0 = stage_finish(p, s, &bar, s_issued, hdr, cnt, true);
   if (n0 < 0) return;
-  append_compute<KDA>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false, kv);
+  append_compute<KDA>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
@@ -945,17 +943,13 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  float kv[16];
-  if (known >= 0) load_record_key(p, s, known, kv);
   bool hdr;
   int cnt;
   stage_start(p, s, known, L, &bar, &s_issued, true, true, p.W - 1, hdr, cnt);
-  const int issued = s_issued;
-  if (known < 0) load_record_key(p, s, issued, kv);
-  const int n0 = stage_finish(p, s, &bar, issued, hdr, cnt, true);
+  const int n0 = stage_finish(p, s, &bar, s_issued, hdr, cnt, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
-  append_compute<KDA>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W, kv);
+  append_compute<KDA>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
   if (n < p.W) {
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
@@ -1061,7 +1055,8 @@ __global__ void __launch_bounds__(256, 2) k_init(Params p) {
 // launchers
 
 static int append_smem(const Params& p) {
-  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W - 1, 0, true, false).end;
+  const int slots = append_slots(p.W, p.phase);
+  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots, slots, true, false).end;
 }
 static int step_smem(const Params& p) {
   return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, p.W, true, true)) + kTailBytes;
