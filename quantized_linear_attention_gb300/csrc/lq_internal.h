@@ -28,6 +28,18 @@ struct Header {
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
+// Byte offsets of one head-state's working set in dynamic shared memory
+// (computed on the host for the kernel being launched).
+struct Stage {
+  // staged by bulk copies, dense
+  int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, q, k, v, alpha_cur;
+  // computed, blocked layout
+  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, line_b, lam_b, kd_b, bd_b, P_b;
+  // computed, dense
+  int basek, baseq, P, g, h, ec, eq, ca;
+  int end;
+};
+
 // Everything a kernel needs, passed by value.
 struct Params {
   int W, C, kda, smooth;
@@ -54,6 +66,8 @@ struct Params {
   float* o;
   const float* S0;  // init source (NULL: zero)
   float* S_out;     // export target
+  Stage st;         // shared-memory layout of the launched kernel
+  int r1;           // bytes of the staging / state-tile region
 };
 
 cudaError_t launch_init(const Params& p, cudaStream_t st);

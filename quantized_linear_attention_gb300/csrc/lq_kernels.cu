@@ -80,6 +80,30 @@ __device__ __forceinline__ float max8(float x) {
   return x;
 }
 
+// Eight quantities at once: v[k] is this lane's block partial of quantity k.
+// Three exchange-and-add steps leave lane qq of the group with the full tree
+// ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)) of quantity 4*(qq&1) + 2*((qq>>1)&1) +
+// ((qq>>2)&1): the same additions as tree8, in the same order, shared out.
+__device__ __forceinline__ float tree8_transpose(const float v[8], int qq) {
+  const bool b0 = (qq & 1) != 0, b1 = (qq & 2) != 0, b2 = (qq & 4) != 0;
+  float s4[4], s2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float keep = b0 ? v[4 + k] : v[k];
+    const float send = b0 ? v[k] : v[4 + k];
+    s4[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float keep = b1 ? s4[2 + k] : s4[k];
+    const float send = b1 ? s4[k] : s4[2 + k];
+    s2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  const float keep = b2 ? s2[1] : s2[0];
+  const float send = b2 ? s2[0] : s2[1];
+  return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+}
+
 // The same tree over 8 partials held in memory.
 __device__ __forceinline__ float tree8_mem(const float* a, int stride) {
   return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[stride]), __fadd_rn(a[2 * stride], a[3 * stride])),
@@ -169,17 +193,6 @@ constexpr int kBV = 160;
 __host__ __device__ __forceinline__ int bv(int j) { return j + ((j >> 4) << 2); }
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
-
-// Byte offsets into dynamic shared memory.
-struct Stage {
-  // staged by bulk copies, dense
-  int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, q, k, v, alpha_cur;
-  // computed, blocked layout
-  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, line_b, lam_b, kd_b, bd_b, P_b;
-  // computed, dense
-  int basek, baseq, P, g, h, ec, eq, ca;
-  int end;
-};
 
 // slots_u: staged record slots of u and alpha; slots_k: staged slots of k (the
 // fold reads every record key; the append reads keys straight into registers).
@@ -515,16 +528,10 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         }
       }
     }
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int i = 32 * pp + 4 * w + r;
-      const float sk = tree8(ak[pp]);
-      const float sq = tree8(aqq[pp]);
-      if (qq == 0) {
-        basek[i] = __fmul_rn(sg[i], sk);
-        baseq[i] = __fmul_rn(sg[i], sq);
-      }
-    }
+    const float v8[8] = {ak[0], ak[1], ak[2], ak[3], aqq[0], aqq[1], aqq[2], aqq[3]};
+    const float tot = tree8_transpose(v8, qq);
+    const int i = 32 * (2 * ((qq >> 1) & 1) + ((qq >> 2) & 1)) + 4 * w + r;
+    ((qq & 1) ? baseq : basek)[i] = __fmul_rn(sg[i], tot);
   }
   __syncthreads();
 
@@ -671,11 +678,28 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   }
 }
 
+// Offsets of the four 16-byte chunks of block qq within row i of the tile
+// (sidx(i, 16qq + 4c4) = 128 i + roff[c4]); they depend on i only through i & 7.
+__device__ __forceinline__ void row_offsets(int i, int qq, int roff[4]) {
+  const int x = (((qq >> 1) + i) & 3) | (i & 4);
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) roff[c4] = ((4 * qq + c4) ^ x) << 2;
+}
+
+// Offsets of column j in a row i with i & 7 == k: sidx(i, j) = 128 i + coff[k].
+__device__ __forceinline__ void column_offsets(int j, int coff[8]) {
+  const int c = j >> 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) coff[k] = ((c ^ ((((c >> 3) + k) & 3) | (k & 4))) << 2) + (j & 3);
+}
+
 // Store a thread's rows into the swizzled tile S; record their row partials
 // ([row][block]) and row scores (squared lengths).
 __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  int roff[4];
+  row_offsets(4 * w + r, qq, roff);  // rows 32pp + 4w + r share i & 7
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
@@ -687,19 +711,20 @@ __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float 
     if (qq == 0) tl.score[i] = rho;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4)
-      *reinterpret_cast<float4*>(&S[sidx(i, 16 * qq + 4 * c4)]) =
+      *reinterpret_cast<float4*>(&S[i * kD + roff[c4]]) =
           make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
   }
   __syncthreads();
 }
 
 // Column block chain: fma (squares) or add (absolute values) over rows
-// 16b..16b+15 of column j, ascending.
+// 16b..16b+15 of column j, ascending (coff from column_offsets(j)).
 template <bool SQUARES>
-__device__ __forceinline__ float column_block(const float* S, int b, int j) {
+__device__ __forceinline__ float column_block(const float* S, int b, const int coff[8]) {
+  const float* base = S + 16 * b * kD;
   float x[16];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) x[t] = S[sidx(16 * b + t, j)];
+  for (int t = 0; t < 16; ++t) x[t] = base[t * kD + coff[t & 7]];
   float acc = 0.0f;
 #pragma unroll
   for (int t = 0; t < 16; ++t) acc = SQUARES ? __fmaf_rn(x[t], x[t], acc) : __fadd_rn(acc, fabsf(x[t]));
@@ -711,10 +736,12 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 
+  int coff[8];
+  column_offsets(tid & (kD - 1), coff);
   // Column scores.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<true>(S, b, j);
+    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<true>(S, b, coff);
   }
   __syncthreads();
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
@@ -756,11 +783,11 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
       // Row win: copy, zero, refresh the column partials of its row block.
       if (tid < kD) {
         const int j = tid;
-        float* e = &S[sidx(win, j)];
+        float* e = &S[win * kD + coff[win & 7]];
         line[j] = *e;
         *e = 0.0f;
         const int b = win >> 4;
-        tl.colpart[b * kD + j] = column_block<true>(S, b, j);
+        tl.colpart[b * kD + j] = column_block<true>(S, b, coff);
         tl.score[kD + j] = tree8_mem(tl.colpart + j, kD);
       } else if (tid < kD + 8) {
         tl.rowpart[win * 8 + (tid - kD)] = 0.0f;
@@ -776,12 +803,17 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         line[i] = *e;
         *e = 0.0f;
         const int q = js >> 4;
-        float x[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) x[t] = S[sidx(i, 16 * q + t)];
+        int ro[4];
+        row_offsets(i, q, ro);
         float pr = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) pr = __fmaf_rn(x[t], x[t], pr);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + ro[c4]]);
+          pr = __fmaf_rn(x.x, x.x, pr);
+          pr = __fmaf_rn(x.y, x.y, pr);
+          pr = __fmaf_rn(x.z, x.z, pr);
+          pr = __fmaf_rn(x.w, x.w, pr);
+        }
         tl.rowpart[i * 8 + q] = pr;
         tl.score[i] = tree8_mem(tl.rowpart + i * 8, 1);
       } else if (tid < kD + 8) {
@@ -796,7 +828,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   // F3: smoothing scales from the residual's column sums of |R|.
   {
     const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<false>(S, b, j);
+    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<false>(S, b, coff);
   }
   __syncthreads();
   if (tid < kD) {
@@ -812,13 +844,15 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     float g[16];
     load16(tl.gsc_b + 20 * qq, g);
     int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
+    int roff[4];
+    row_offsets(4 * w + r, qq, roff);
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
       float t[16];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const float4 x = *reinterpret_cast<const float4*>(&S[sidx(i, 16 * qq + 4 * c4)]);
+        const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
         t[4 * c4 + 0] = x.x;
         t[4 * c4 + 1] = x.y;
         t[4 * c4 + 2] = x.z;
@@ -861,31 +895,41 @@ namespace lqi {
 extern __shared__ __align__(128) char lq_dyn_smem[];
 
 // Thread 0 starts the copies (at once when `known_n0` >= 0, else after reading
-// the record count) and publishes the count it used in *s_issued; every thread
-// reads the header and the count meanwhile. Returns after the __syncthreads
-// that publishes *s_issued.
-__device__ __forceinline__ void stage_start(const Params& p, int64_t s, int known_n0, const Stage& L, uint64_t* bar,
-                                            int* s_issued, bool append, bool stage_k, int max_n0, bool& hdr,
-                                            int& cnt) {
+// the record count), checks the header and publishes what it found in shared
+// memory; returns after the __syncthreads that makes it visible.
+struct StageInfo {
+  int issued;  // record count the copies were issued for, or -1
+  int cnt;     // record count read from the state
+  int hdr;     // header matches this configuration
+};
+
+__device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int known_n0, const Stage& L,
+                                                 uint64_t* bar, StageInfo* sh, bool append, bool stage_k,
+                                                 int max_n0) {
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     int n0 = known_n0;
-    if (n0 < 0) {
-      const int c = p.counts[s];
-      n0 = (c >= 0 && c <= max_n0) ? c : -1;
-    }
     if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append, stage_k);
-    *s_issued = n0;
+    const int c = p.counts[s];
+    const int h = header_ok(p) ? 1 : 0;
+    if (n0 < 0) {
+      n0 = (h && c >= 0 && c <= max_n0) ? c : -1;
+      if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append, stage_k);
+    }
+    sh->issued = n0;
+    sh->cnt = c;
+    sh->hdr = h;
   }
-  hdr = header_ok(p);
-  cnt = p.counts[s];
   __syncthreads();
+  return *sh;
 }
 
 // Bounded wait for the copies, then the checks. Returns the record count held
 // (>= 0) or -1 after recording an error; uniform over the CTA.
-__device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t* bar, int n0, bool hdr, int cnt,
+__device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t* bar, const StageInfo& si,
                                             bool append) {
+  const int n0 = si.issued, cnt = si.cnt;
+  const bool hdr = si.hdr != 0;
   if (n0 >= 0) {
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -917,17 +961,15 @@ __host__ __device__ inline int append_slots(int W, int phase) { return (phase >=
 template <bool KDA>
 __global__ void __launch_bounds__(256, 6) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_issued;
+  __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
   const int slots = append_slots(p.W, p.phase);
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, slots, slots, true, false);
+  const Stage& L = p.st;
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  bool hdr;
-  int cnt;
-  stage_start(p, s, known, L, &bar, &s_issued, true, true, slots, hdr, cnt);
-  const int n0 = stage_finish(p, s, &bar, s_issued, hdr, cnt, true);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, slots);
+  const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   append_compute<KDA>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
@@ -937,16 +979,14 @@ __global__ void __launch_bounds__(256, 6) k_append(Params p) {
 template <bool KDA>
 __global__ void __launch_bounds__(256, 2) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_issued;
+  __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, true, true);
+  const Stage& L = p.st;
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  bool hdr;
-  int cnt;
-  stage_start(p, s, known, L, &bar, &s_issued, true, true, p.W - 1, hdr, cnt);
-  const int n0 = stage_finish(p, s, &bar, s_issued, hdr, cnt, true);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, p.W - 1);
+  const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
   append_compute<KDA>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
@@ -959,7 +999,7 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
   float acc[4][16];
   reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
-  const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
+  const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
   boundary_from_tile(p, s, S, tl);
@@ -969,13 +1009,11 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
 template <bool KDA>
 __global__ void __launch_bounds__(256, 2) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_issued;
+  __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, false, true);
-  bool hdr;
-  int cnt;
-  stage_start(p, s, -1, L, &bar, &s_issued, false, true, p.W, hdr, cnt);
-  const int n = stage_finish(p, s, &bar, s_issued, hdr, cnt, false);
+  const Stage& L = p.st;
+  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, false, true, p.W);
+  const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
                       at<float>(lq_dyn_smem, L.P_b));
@@ -984,7 +1022,7 @@ __global__ void __launch_bounds__(256, 2) k_fold(Params p) {
   float acc[4][16];
   reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();
-  const Tail tl = carve_tail(lq_dyn_smem, region1_bytes(L));
+  const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
   boundary_from_tile(p, s, S, tl);
@@ -994,15 +1032,13 @@ __global__ void __launch_bounds__(256, 2) k_fold(Params p) {
 template <bool KDA>
 __global__ void __launch_bounds__(256, 2) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_issued;
+  __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
-  const Stage L = stage_layout(p.W, p.C, KDA, (int)p.comp_id_stride, p.W, p.W, false, true);
-  bool hdr;
-  int cnt;
-  stage_start(p, s, -1, L, &bar, &s_issued, false, true, p.W, hdr, cnt);
-  const int n = stage_finish(p, s, &bar, s_issued, hdr, cnt, false);
+  const Stage& L = p.st;
+  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, false, true, p.W);
+  const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
                       at<float>(lq_dyn_smem, L.P_b));
@@ -1045,7 +1081,7 @@ __global__ void __launch_bounds__(256, 2) k_init(Params p) {
       for (int t = 0; t < 16; ++t) acc[pp][t] = 0.0f;
     }
   }
-  const Tail tl = carve_tail(lq_dyn_smem, kTileBytes);
+  const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
   boundary_from_tile(p, s, S, tl);
@@ -1054,16 +1090,13 @@ __global__ void __launch_bounds__(256, 2) k_init(Params p) {
 // ---------------------------------------------------------------------------
 // launchers
 
-static int append_smem(const Params& p) {
-  const int slots = append_slots(p.W, p.phase);
-  return stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots, slots, true, false).end;
+static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile) {
+  Params q = p;
+  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold);
+  q.r1 = tile ? region1_bytes(q.st) : q.st.end;
+  return q;
 }
-static int step_smem(const Params& p) {
-  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, p.W, true, true)) + kTailBytes;
-}
-static int fold_smem(const Params& p) {
-  return region1_bytes(stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, p.W, p.W, false, true)) + kTailBytes;
-}
+static int smem_of(const Params& q, bool tile) { return tile ? q.r1 + kTailBytes : q.st.end; }
 
 template <typename K>
 static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st) {
@@ -1073,22 +1106,30 @@ static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-cudaError_t launch_init(const Params& p, cudaStream_t st) { return launch(k_init, p, kTileBytes + kTailBytes, st); }
+cudaError_t launch_init(const Params& p, cudaStream_t st) {
+  const Params q = with_layout(p, 0, 0, false, false, true);
+  return launch(k_init, q, smem_of(q, true), st);
+}
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_append<true>, p, append_smem(p), st) : launch(k_append<false>, p, append_smem(p), st);
+  const int slots = append_slots(p.W, p.phase);
+  const Params q = with_layout(p, slots, slots, true, false, false);
+  return p.kda ? launch(k_append<true>, q, smem_of(q, false), st) : launch(k_append<false>, q, smem_of(q, false), st);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_step<true>, p, step_smem(p), st) : launch(k_step<false>, p, step_smem(p), st);
+  const Params q = with_layout(p, p.W, p.W, true, true, true);
+  return p.kda ? launch(k_step<true>, q, smem_of(q, true), st) : launch(k_step<false>, q, smem_of(q, true), st);
 }
 
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_fold<true>, p, fold_smem(p), st) : launch(k_fold<false>, p, fold_smem(p), st);
+  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  return p.kda ? launch(k_fold<true>, q, smem_of(q, true), st) : launch(k_fold<false>, q, smem_of(q, true), st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {
-  return p.kda ? launch(k_export<true>, p, fold_smem(p), st) : launch(k_export<false>, p, fold_smem(p), st);
+  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  return p.kda ? launch(k_export<true>, q, smem_of(q, true), st) : launch(k_export<false>, q, smem_of(q, true), st);
 }
 
 }  // namespace lqi
