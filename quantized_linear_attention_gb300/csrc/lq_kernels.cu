@@ -104,6 +104,26 @@ __device__ __forceinline__ float tree8_transpose(const float v[8], int qq) {
   return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 4));
 }
 
+// Q quantities (Q = 8 or 16) at once: v[k] is this lane's block partial of
+// quantity k. Three exchange-and-add steps (partners lane^1, ^2, ^4) leave lane
+// qq with the full trees of quantities (Q/2)b0 + (Q/4)b1 + (Q/8)b2 + e,
+// e < Q/8 (b = the bits of qq): the additions of tree8, in its order.
+template <int Q>
+__device__ __forceinline__ void tree_transpose(float v[Q], int qq, float out[Q / 8]) {
+#pragma unroll
+  for (int st = 0, cnt = Q; st < 3; ++st, cnt >>= 1) {
+    const bool hi = ((qq >> st) & 1) != 0;
+#pragma unroll
+    for (int k = 0; k < cnt / 2; ++k) {
+      const float keep = hi ? v[cnt / 2 + k] : v[k];
+      const float send = hi ? v[k] : v[cnt / 2 + k];
+      v[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1 << st));
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < Q / 8; ++e) out[e] = v[e];
+}
+
 // The same tree over 8 partials held in memory.
 __device__ __forceinline__ float tree8_mem(const float* a, int stride) {
   return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[stride]), __fadd_rn(a[2 * stride], a[3 * stride])),
@@ -361,16 +381,19 @@ __device__ __forceinline__ float decay_at(const float* P, const float* P_b, int 
 
 // ---------------------------------------------------------------------------
 // Append (A0-A7): one token into head-state s holding n-1 records, inputs
-// staged in shared memory. LeapQuant §3.2 (outputs from the fixed low-bit state plus
-// buffered records), App. B.2 (base term O(d_k d_v), each record
+// staged in shared memory. LeapQuant §3.2 (outputs from the fixed low-bit state
+// plus buffered records), App. B.2 (base term O(d_k d_v), each record
 // O(d_k + d_v)), App. B.3 (the smoothing scales act on the residual term only),
 // §3.3 (compensators are records at window position 0 carrying the full decay).
 // With `fold_follows`, the new record is also left in the staged buffers.
-// 256 threads: lane group (w, r) owns rows 32pp + 4w + r, lane qq owns the
-// 16-element block qq of every vector.
-template <bool KDA>
+// NT threads (128 or 256); lane group (w, r) owns rows pp * 4 * (NT/32) + 4w + r,
+// lane qq owns the 16-element block qq of every vector.
+template <bool KDA, int NT>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                float alpha_scalar, float beta, bool fold_follows) {
+  constexpr int NW = NT / 32;
+  constexpr int RPT = 128 / (4 * NW);  // rows per thread: 8 or 4
+  constexpr int NG = NT / 8;           // lane groups
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   float* P = at<float>(sm, L.P);
@@ -390,20 +413,39 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   float* h = at<float>(sm, L.h);
   float* ec = at<float>(sm, L.ec);
   float* eq = at<float>(sm, L.eq);
+  const float* ra = at<float>(sm, L.rec_alpha);
   const float* sg = at<float>(sm, L.sigma);
   const float* lam = at<float>(sm, L.lambda);
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
 
-  // A0: decay products over records 1..n-1 and this token's alpha.
-  decay_products<KDA>(n, at<float>(sm, L.rec_alpha), at<float>(sm, L.alpha_cur), alpha_scalar, true, P, P_b);
-  __syncthreads();
-
-  // A1: y = A_n . k_n; z = lambda . y (and the same for q, for the output);
-  // blocked copies of k_n, q_n and the compensator lines for the dot products.
+  // A0 + A1. Decay products P_n = 1, P_{m-1} = P_m * alpha_m (backward running
+  // products over records 1..n-1 and this token's alpha). KDA: thread j runs
+  // column j's chain. GDN: every thread of the first 128 runs the scalar chain
+  // (it needs P_0), thread 0 keeps the table. Then y = A_n . k_n,
+  // z = lambda . y, and blocked copies for the dot products.
   if (tid < kD) {
     const int j = tid, jb = bv(j);
-    const float A = decay_at<KDA>(P, P_b, 0, j);
+    float A;
+    if (KDA) {
+      const float* ac = at<float>(sm, L.alpha_cur);
+      float pr = 1.0f;
+      P_b[n * kBV + jb] = pr;
+      for (int m = n; m >= 1; --m) {
+        pr = __fmul_rn(pr, m == n ? ac[j] : ra[(m - 1) * kD + j]);
+        P_b[(m - 1) * kBV + jb] = pr;
+      }
+      A = pr;
+    } else {
+      float pr = 1.0f;
+      if (j == 0) P[n] = pr;
+#pragma unroll 8
+      for (int m = n; m >= 1; --m) {
+        pr = __fmul_rn(pr, m == n ? alpha_scalar : ra[m - 1]);
+        if (j == 0) P[m - 1] = pr;
+      }
+      A = pr;
+    }
     const float kj = kn[j], qj = qn[j];
     const float yy = __fmul_rn(A, kj);
     const float qa = __fmul_rn(A, qj);
@@ -413,19 +455,19 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     aq_b[jb] = qa;
     zk_b[jb] = __fmul_rn(lam[j], yy);
     zq_b[jb] = __fmul_rn(lam[j], qa);
-  } else {
-    const int j = tid - kD, jb = bv(j);
-    for (int c = 0; c < p.C; ++c) line_b[c * kBV + jb] = cl[c * kD + j];
   }
+  for (int e = (NT > kD ? tid - kD : tid); e >= 0 && e < p.C * kD; e += kD)
+    line_b[(e >> 7) * kBV + bv(e & (kD - 1))] = cl[e];
   __syncthreads();
 
   // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
   // compensators, then k_n . q_n (the new record's output term, P_n = 1).
+  // The k-side sums (g, ec) are pinned; the q-side (h, eq) only feeds o.
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
     const int njobs = nrec + p.C + 1;
-    for (int base = 0; base < njobs; base += 32) {
+    for (int base = 0; base < njobs; base += NG) {
       const int job = base + grp;
       float pa = 0.0f, pb = 0.0f;
       if (job < njobs) {
@@ -439,14 +481,22 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const float4 kvc = kv4[c4], kx = kx4[c4], qx = qx4[c4];
-            const float4 pm = KDA ? pm4[c4] : make_float4(pms, pms, pms, pms);
             const float kvs[4] = {kvc.x, kvc.y, kvc.z, kvc.w};
             const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
-            const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
+            if (KDA) {
+              const float4 pm = pm4[c4];
+              const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pa = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], kxs[e]), pa);
-              pb = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], qxs[e]), pb);
+              for (int e = 0; e < 4; ++e) {
+                pa = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], kxs[e]), pa);
+                pb = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], qxs[e]), pb);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                pa = __fmaf_rn(kvs[e], __fmul_rn(pms, kxs[e]), pa);
+                pb = __fmaf_rn(kvs[e], qxs[e], pb);  // scaled by P_m after the tree
+              }
             }
           }
         } else if (job < nrec + p.C) {
@@ -485,7 +535,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       if (job < njobs && qq == 0) {
         if (job < nrec) {
           g[job + 1] = pa;
-          h[job + 1] = pb;
+          h[job + 1] = KDA ? pb : __fmul_rn(P[job + 1], pb);
         } else if (job < nrec + p.C) {
           ec[job - nrec] = pa;
           eq[job - nrec] = pb;
@@ -498,45 +548,63 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
 
   // A2: fused dequantize + two matvecs: one 16-byte code load per row, exact
   // conversions and 2 fmas per code. The z blocks are consumed 4 elements at a
-  // time with the thread's 4 rows interleaved; each row's chain still runs over
-  // its 16 elements in ascending order, then the tree.
+  // time, 4 rows interleaved; each row's chain runs over its 16 elements in
+  // ascending order, then the canonical tree (shared out over the lane group).
   {
     const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
-    uint32_t cw[4][4];
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int4 c = *reinterpret_cast<const int4*>(cb + (32 * pp + 4 * w + r) * kD);
-      cw[pp][0] = (uint32_t)c.x ^ 0x80808080u;
-      cw[pp][1] = (uint32_t)c.y ^ 0x80808080u;
-      cw[pp][2] = (uint32_t)c.z ^ 0x80808080u;
-      cw[pp][3] = (uint32_t)c.w ^ 0x80808080u;
-    }
-    float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
     const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
+    float v[2 * RPT];
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const float4 a = zk4[c4], b = zq4[c4];
-      const float za[4] = {a.x, a.y, a.z, a.w}, zb[4] = {b.x, b.y, b.z, b.w};
+    for (int half = 0; half < RPT / 4; ++half) {
+      uint32_t cw[4][4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
+        const int4 c = *reinterpret_cast<const int4*>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * kD);
+        cw[pp][0] = (uint32_t)c.x ^ 0x80808080u;
+        cw[pp][1] = (uint32_t)c.y ^ 0x80808080u;
+        cw[pp][2] = (uint32_t)c.z ^ 0x80808080u;
+        cw[pp][3] = (uint32_t)c.w ^ 0x80808080u;
+      }
+      float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float f = code_f(cw[pp][c4], e);
-          ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
-          aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 a = zk4[c4], b = zq4[c4];
+        const float za[4] = {a.x, a.y, a.z, a.w}, zb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f = code_f(cw[pp][c4], e);
+            ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
+            aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
+          }
         }
       }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        v[4 * half + pp] = ak[pp];
+        v[RPT + 4 * half + pp] = aqq[pp];
+      }
     }
-    const float v8[8] = {ak[0], ak[1], ak[2], ak[3], aqq[0], aqq[1], aqq[2], aqq[3]};
-    const float tot = tree8_transpose(v8, qq);
-    const int i = 32 * (2 * ((qq >> 1) & 1) + ((qq >> 2) & 1)) + 4 * w + r;
-    ((qq & 1) ? baseq : basek)[i] = __fmul_rn(sg[i], tot);
+    float tot[2 * RPT / 8];
+    tree_transpose<2 * RPT>(v, qq, tot);
+    // lane qq now holds quantities RPT*b0 + (RPT/2)*b1 + (RPT/4)*b2 + e
+    const int b0 = qq & 1, b1 = (qq >> 1) & 1, b2 = (qq >> 2) & 1;
+    float* dst = b0 ? baseq : basek;
+#pragma unroll
+    for (int e = 0; e < 2 * RPT / 8; ++e) {
+      const int pp = (RPT / 2) * b1 + (RPT / 4) * b2 + e;
+      const int i = pp * 4 * NW + 4 * w + r;
+      dst[i] = __fmul_rn(sg[i], tot[e]);
+    }
   }
   __syncthreads();
 
   // A3-A5 per value row: acc = base; compensators in order; records in order;
   // u_n = beta (v - acc). A6: the output in any order. A7: store record n.
+  // A row compensator's coefficient a_c[i] is zero except on its own row, and
+  // fma(0, x, acc) returns acc for the finite, never negative-zero acc here.
   float* ru = at<float>(sm, L.rec_u);
   const float* vv = at<float>(sm, L.v);
   if (tid < kD) {
@@ -545,9 +613,14 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     float oo = baseq[i];
     for (int c = 0; c < p.C; ++c) {
       const int id = cid[c];
-      const float a = (id < kD) ? (i == id ? 1.0f : 0.0f) : cl[c * kD + i];
-      acc = __fmaf_rn(a, ec[c], acc);
-      oo = __fmaf_rn(a, eq[c], oo);
+      if (id >= kD) {
+        const float a = cl[c * kD + i];
+        acc = __fmaf_rn(a, ec[c], acc);
+        oo = __fmaf_rn(a, eq[c], oo);
+      } else if (id == i) {
+        acc = __fmaf_rn(1.0f, ec[c], acc);
+        oo = __fmaf_rn(1.0f, eq[c], oo);
+      }
     }
 #pragma unroll 4
     for (int m = 1; m <= n - 1; ++m) {
@@ -560,8 +633,9 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     p.rec_u[(s * p.W + (n - 1)) * kD + i] = u;
     p.o[s * kD + i] = oo;
     if (fold_follows) ru[(n - 1) * kD + i] = u;
-  } else {
-    const int j = tid - kD;
+  }
+  if (NT == kD || tid >= kD) {
+    const int j = NT == kD ? tid : tid - kD;
     p.rec_k[(s * p.W + (n - 1)) * kD + j] = kn[j];
     if (fold_follows) at<float>(sm, L.rec_k)[(n - 1) * kD + j] = kn[j];
     if (KDA)
@@ -623,7 +697,6 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   const float* P = at<float>(sm, L.P);
   const float* P_b = at<float>(sm, L.P_b);
   const float* sg = at<float>(sm, L.sigma);
-  const float* ca = at<float>(sm, L.ca);
   const float* bd_b = at<float>(sm, L.bd_b);
   const float* kd_b = at<float>(sm, L.kd_b);
   const float* U = at<float>(sm, L.rec_u);
@@ -642,20 +715,56 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
       for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[t]), lam[t]), p0[t]);
     }
   }
+  // Compensators in order. The term fma(a_c[i], (P_0 . b_c)[j], S_ij) has a
+  // zero coefficient everywhere except on the compensator's own line, and there
+  // it returns S_ij unchanged (S is finite and never negative zero here), so
+  // only that line is touched: a row compensator adds P_0 . line to its row, a
+  // column compensator j0 adds line[i] * P_0[j0] to column j0.
+  const int32_t* cid = at<int32_t>(sm, L.comp_id);
+  const float* cl = at<float>(sm, L.comp_line);
   for (int c = 0; c < p.C; ++c) {
-    float a[4];
+    const int id = cid[c];
+    if (id < kD) {
+      if (((id & 31) >> 2) == w) {  // warp-uniform: row id is one of this warp's rows
+        const int pp_own = id >> 5;
+        if ((id & 3) == r) {
+          const float4* b4 = reinterpret_cast<const float4*>(bd_b + c * kBV + 20 * qq);
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) a[pp] = ca[c * kD + 32 * pp + 4 * w + r];
-    const float4* b4 = reinterpret_cast<const float4*>(bd_b + c * kBV + 20 * qq);
+          for (int pp = 0; pp < 4; ++pp) {
+            if (pp != pp_own) continue;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const float4 b = b4[c4];
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 b = b4[c4];
+              acc[pp][4 * c4 + 0] = __fmaf_rn(1.0f, b.x, acc[pp][4 * c4 + 0]);
+              acc[pp][4 * c4 + 1] = __fmaf_rn(1.0f, b.y, acc[pp][4 * c4 + 1]);
+              acc[pp][4 * c4 + 2] = __fmaf_rn(1.0f, b.z, acc[pp][4 * c4 + 2]);
+              acc[pp][4 * c4 + 3] = __fmaf_rn(1.0f, b.w, acc[pp][4 * c4 + 3]);
+            }
+          }
+        }
+      }
+    } else {
+      const int j0 = id - kD;
+      if (qq == (j0 >> 4)) {
+        const float pj = KDA ? P_b[bv(j0)] : P[0];
+        float li[4];
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        acc[pp][4 * c4 + 0] = __fmaf_rn(a[pp], b.x, acc[pp][4 * c4 + 0]);
-        acc[pp][4 * c4 + 1] = __fmaf_rn(a[pp], b.y, acc[pp][4 * c4 + 1]);
-        acc[pp][4 * c4 + 2] = __fmaf_rn(a[pp], b.z, acc[pp][4 * c4 + 2]);
-        acc[pp][4 * c4 + 3] = __fmaf_rn(a[pp], b.w, acc[pp][4 * c4 + 3]);
+        for (int pp = 0; pp < 4; ++pp) li[pp] = cl[c * kD + 32 * pp + 4 * w + r];
+        switch (j0 & 15) {
+#define LQ_COLCOMP(T)                                                                   \
+  case T:                                                                              \
+    acc[0][T] = __fmaf_rn(li[0], pj, acc[0][T]);                                       \
+    acc[1][T] = __fmaf_rn(li[1], pj, acc[1][T]);                                       \
+    acc[2][T] = __fmaf_rn(li[2], pj, acc[2][T]);                                       \
+    acc[3][T] = __fmaf_rn(li[3], pj, acc[3][T]);                                       \
+    break;
+          LQ_COLCOMP(0) LQ_COLCOMP(1) LQ_COLCOMP(2) LQ_COLCOMP(3) LQ_COLCOMP(4) LQ_COLCOMP(5) LQ_COLCOMP(6)
+          LQ_COLCOMP(7) LQ_COLCOMP(8) LQ_COLCOMP(9) LQ_COLCOMP(10) LQ_COLCOMP(11) LQ_COLCOMP(12)
+          LQ_COLCOMP(13) LQ_COLCOMP(14) LQ_COLCOMP(15)
+#undef LQ_COLCOMP
+          default:
+            break;
+        }
       }
     }
   }
@@ -871,13 +980,17 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         hh = __fdiv_rn(127.0f, mx);
       }
       if (qq == 0) p.sigma[s * kD + i] = sgm;
-      uint32_t wd[4] = {0u, 0u, 0u, 0u};
+      // Round t*h to the nearest integer, ties to even: |t*h| <= 127(1+2^-24)^2
+      // < 127.5, so adding 1.5 * 2^23 leaves the integer, in [-127, 127], in
+      // the low mantissa bits (two's complement), and no clamp is needed.
+      uint32_t rb[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        int cq = __float2int_rn(__fmul_rn(t[e], hh));
-        cq = min(max(cq, -127), 127);
-        wd[e >> 2] |= ((uint32_t)cq & 0xFFu) << (8 * (e & 3));
-      }
+      for (int e = 0; e < 16; ++e) rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[e], hh), 12582912.0f));
+      uint32_t wd[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        wd[q4] = __byte_perm(__byte_perm(rb[4 * q4], rb[4 * q4 + 1], 0x0040u),
+                             __byte_perm(rb[4 * q4 + 2], rb[4 * q4 + 3], 0x0040u), 0x5410u);
       *reinterpret_cast<int4*>(cbase + i * kD) = make_int4((int)wd[0], (int)wd[1], (int)wd[2], (int)wd[3]);
     }
   }
@@ -959,7 +1072,7 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
 __host__ __device__ inline int append_slots(int W, int phase) { return (phase >= 0 && phase < W) ? phase : W - 1; }
 
 template <bool KDA>
-__global__ void __launch_bounds__(256, 6) k_append(Params p) {
+__global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -971,7 +1084,7 @@ __global__ void __launch_bounds__(256, 6) k_append(Params p) {
   const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, slots);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
+  append_compute<KDA, 128>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
@@ -989,7 +1102,7 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
-  append_compute<KDA>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
+  append_compute<KDA, 256>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
   if (n < p.W) {
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
@@ -1099,10 +1212,10 @@ static Params with_layout(const Params& p, int slots_u, int slots_k, bool append
 static int smem_of(const Params& q, bool tile) { return tile ? q.r1 + kTailBytes : q.st.end; }
 
 template <typename K>
-static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st) {
+static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, int threads = 256) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3((unsigned)p.n_states), dim3(256), (size_t)smem, st>>>(p);
+  kernel<<<dim3((unsigned)p.n_states), dim3(threads), (size_t)smem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -1114,7 +1227,8 @@ cudaError_t launch_init(const Params& p, cudaStream_t st) {
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const int slots = append_slots(p.W, p.phase);
   const Params q = with_layout(p, slots, slots, true, false, false);
-  return p.kda ? launch(k_append<true>, q, smem_of(q, false), st) : launch(k_append<false>, q, smem_of(q, false), st);
+  return p.kda ? launch(k_append<true>, q, smem_of(q, false), st, 128)
+               : launch(k_append<false>, q, smem_of(q, false), st, 128);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
