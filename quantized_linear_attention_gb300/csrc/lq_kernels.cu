@@ -244,7 +244,7 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.aq_b = take(va * 4 * kBV);
   L.zk_b = take(va * 4 * kBV);
   L.zq_b = take(va * 4 * kBV);
-  L.line_b = take(va * 4 * kBV * C);
+  L.line_b = take(0);
   L.lam_b = take(fo * 4 * kBV);
   L.kd_b = take(fo * 4 * kBV * W);
   L.bd_b = take(fo * 4 * kBV * C);
@@ -385,12 +385,12 @@ __device__ __forceinline__ float decay_at(const float* P, const float* P_b, int 
 // plus buffered records), App. B.2 (base term O(d_k d_v), each record
 // O(d_k + d_v)), App. B.3 (the smoothing scales act on the residual term only),
 // §3.3 (compensators are records at window position 0 carrying the full decay).
-// With `fold_follows`, the new record is also left in the staged buffers.
+// With FOLD (the window fills), the new record is also left in the staged buffers.
 // NT threads (128 or 256); lane group (w, r) owns rows pp * 4 * (NT/32) + 4w + r,
 // lane qq owns the 16-element block qq of every vector.
-template <bool KDA, int NT>
+template <bool KDA, int NT, bool FOLD>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
-                                               float alpha_scalar, float beta, bool fold_follows) {
+                                               float alpha_scalar, float beta) {
   constexpr int NW = NT / 32;
   constexpr int RPT = 128 / (4 * NW);  // rows per thread: 8 or 4
   constexpr int NG = NT / 8;           // lane groups
@@ -406,7 +406,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   float* aq_b = at<float>(sm, L.aq_b);
   float* zk_b = at<float>(sm, L.zk_b);
   float* zq_b = at<float>(sm, L.zq_b);
-  float* line_b = at<float>(sm, L.line_b);
   float* basek = at<float>(sm, L.basek);
   float* baseq = at<float>(sm, L.baseq);
   float* g = at<float>(sm, L.g);
@@ -419,33 +418,39 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
 
-  // A0 + A1. Decay products P_n = 1, P_{m-1} = P_m * alpha_m (backward running
+  // A0: decay products P_n = 1, P_{m-1} = P_m * alpha_m (backward running
   // products over records 1..n-1 and this token's alpha). KDA: thread j runs
-  // column j's chain. GDN: every thread of the first 128 runs the scalar chain
-  // (it needs P_0), thread 0 keeps the table. Then y = A_n . k_n,
-  // z = lambda . y, and blocked copies for the dot products.
-  if (tid < kD) {
-    const int j = tid, jb = bv(j);
-    float A;
-    if (KDA) {
+  // column j's chain (it uses only its own column below). GDN: thread 0 runs
+  // the scalar chain into the table.
+  if (KDA) {
+    if (tid < kD) {
       const float* ac = at<float>(sm, L.alpha_cur);
+      const int jb = bv(tid);
       float pr = 1.0f;
       P_b[n * kBV + jb] = pr;
       for (int m = n; m >= 1; --m) {
-        pr = __fmul_rn(pr, m == n ? ac[j] : ra[(m - 1) * kD + j]);
+        pr = __fmul_rn(pr, m == n ? ac[tid] : ra[(m - 1) * kD + tid]);
         P_b[(m - 1) * kBV + jb] = pr;
       }
-      A = pr;
-    } else {
-      float pr = 1.0f;
-      if (j == 0) P[n] = pr;
-#pragma unroll 8
-      for (int m = n; m >= 1; --m) {
-        pr = __fmul_rn(pr, m == n ? alpha_scalar : ra[m - 1]);
-        if (j == 0) P[m - 1] = pr;
-      }
-      A = pr;
     }
+  } else {
+    if (tid == 0) {
+      float pr = 1.0f;
+      P[n] = pr;
+      pr = __fmul_rn(pr, alpha_scalar);
+      P[n - 1] = pr;
+#pragma unroll 4
+      for (int m = n - 1; m >= 1; --m) {
+        pr = __fmul_rn(pr, ra[m - 1]);
+        P[m - 1] = pr;
+      }
+    }
+    __syncthreads();
+  }
+  // A1: y = A_n . k_n, z = lambda . y, and blocked copies for the dot products.
+  if (tid < kD) {
+    const int j = tid, jb = bv(j);
+    const float A = KDA ? P_b[jb] : P[0];
     const float kj = kn[j], qj = qn[j];
     const float yy = __fmul_rn(A, kj);
     const float qa = __fmul_rn(A, qj);
@@ -456,8 +461,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     zk_b[jb] = __fmul_rn(lam[j], yy);
     zq_b[jb] = __fmul_rn(lam[j], qa);
   }
-  for (int e = (NT > kD ? tid - kD : tid); e >= 0 && e < p.C * kD; e += kD)
-    line_b[(e >> 7) * kBV + bv(e & (kD - 1))] = cl[e];
   __syncthreads();
 
   // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
@@ -502,7 +505,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         } else if (job < nrec + p.C) {
           const int c = job - nrec;
           const int id = cid[c];
-          const float4* b4 = reinterpret_cast<const float4*>(line_b + c * kBV + 20 * qq);
+          const float4* b4 = reinterpret_cast<const float4*>(cl + c * kD + 16 * qq);
           const float4* y4 = reinterpret_cast<const float4*>(y_b + 20 * qq);
           const float4* a4 = reinterpret_cast<const float4*>(aq_b + 20 * qq);
 #pragma unroll
@@ -607,6 +610,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // fma(0, x, acc) returns acc for the finite, never negative-zero acc here.
   float* ru = at<float>(sm, L.rec_u);
   const float* vv = at<float>(sm, L.v);
+  const int64_t rec_off = (s * p.W + (n - 1)) * kD;  // record slot n-1 of head-state s
   if (tid < kD) {
     const int i = tid;
     float acc = basek[i];
@@ -622,22 +626,23 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         oo = __fmaf_rn(1.0f, eq[c], oo);
       }
     }
+    const float* rui = ru + i;
 #pragma unroll 4
     for (int m = 1; m <= n - 1; ++m) {
-      const float um = ru[(m - 1) * kD + i];
+      const float um = rui[(m - 1) * kD];
       acc = __fmaf_rn(um, g[m], acc);
       oo = __fmaf_rn(um, h[m], oo);
     }
     const float u = __fmul_rn(beta, __fsub_rn(vv[i], acc));
     oo = __fmaf_rn(u, h[n], oo);
-    p.rec_u[(s * p.W + (n - 1)) * kD + i] = u;
+    p.rec_u[rec_off + i] = u;
     p.o[s * kD + i] = oo;
-    if (fold_follows) ru[(n - 1) * kD + i] = u;
+    if (FOLD) ru[(n - 1) * kD + i] = u;
   }
   if (NT == kD || tid >= kD) {
     const int j = NT == kD ? tid : tid - kD;
-    p.rec_k[(s * p.W + (n - 1)) * kD + j] = kn[j];
-    if (fold_follows) at<float>(sm, L.rec_k)[(n - 1) * kD + j] = kn[j];
+    p.rec_k[rec_off + j] = kn[j];
+    if (FOLD) at<float>(sm, L.rec_k)[(n - 1) * kD + j] = kn[j];
     if (KDA)
       p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + j] = at<float>(sm, L.alpha_cur)[j];
     else if (j == 0)
@@ -840,6 +845,36 @@ __device__ __forceinline__ float column_block(const float* S, int b, const int c
   return acc;
 }
 
+// Block partials of every column (SQUARES: fma chains of squares; else add
+// chains of absolute values), 256 threads: thread (b, cq) covers columns
+// 4cq..4cq+3 of rows 16b..16b+15 in ascending row order, one 16-byte load per
+// row. A warp reads whole rows, and the swizzle spreads them over all banks.
+template <bool SQUARES>
+__device__ __forceinline__ void column_quads(const float* S, float* colpart) {
+  const int b = threadIdx.x >> 5, cq = threadIdx.x & 31;
+  int off[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) off[k] = (cq ^ ((((cq >> 3) + k) & 3) | (k & 4))) << 2;
+  const float* base = S + 16 * b * kD;
+  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const float4 x = *reinterpret_cast<const float4*>(base + t * kD + off[t & 7]);
+    if (SQUARES) {
+      a0 = __fmaf_rn(x.x, x.x, a0);
+      a1 = __fmaf_rn(x.y, x.y, a1);
+      a2 = __fmaf_rn(x.z, x.z, a2);
+      a3 = __fmaf_rn(x.w, x.w, a3);
+    } else {
+      a0 = __fadd_rn(a0, fabsf(x.x));
+      a1 = __fadd_rn(a1, fabsf(x.y));
+      a2 = __fadd_rn(a2, fabsf(x.z));
+      a3 = __fadd_rn(a3, fabsf(x.w));
+    }
+  }
+  *reinterpret_cast<float4*>(colpart + b * kD + 4 * cq) = make_float4(a0, a1, a2, a3);
+}
+
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
 __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
   const int tid = threadIdx.x;
@@ -847,11 +882,9 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
 
   int coff[8];
   column_offsets(tid & (kD - 1), coff);
-  // Column scores.
-  {
-    const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<true>(S, b, coff);
-  }
+  // Column scores: thread (b = tid / 32, quad cq = tid % 32) runs the four
+  // chains of columns 4cq..4cq+3 over rows 16b..16b+15 with 16-byte loads.
+  column_quads<true>(S, tl.colpart);
   __syncthreads();
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
@@ -935,10 +968,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   }
 
   // F3: smoothing scales from the residual's column sums of |R|.
-  {
-    const int j = tid & (kD - 1);
-    for (int b = tid >> 7; b < 8; b += 2) tl.colpart[b * kD + j] = column_block<false>(S, b, coff);
-  }
+  column_quads<false>(S, tl.colpart);
   __syncthreads();
   if (tid < kD) {
     const float mu = __fmul_rn(tree8_mem(tl.colpart + tid, kD), 1.0f / (float)kD);
@@ -955,37 +985,53 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
     int roff[4];
     row_offsets(4 * w + r, qq, roff);
+    float t[4][16], mx[4];
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
-      float t[16];
+      mx[pp] = 0.0f;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
-        t[4 * c4 + 0] = x.x;
-        t[4 * c4 + 1] = x.y;
-        t[4 * c4 + 2] = x.z;
-        t[4 * c4 + 3] = x.w;
+        t[pp][4 * c4 + 0] = __fmul_rn(x.x, g[4 * c4 + 0]);
+        t[pp][4 * c4 + 1] = __fmul_rn(x.y, g[4 * c4 + 1]);
+        t[pp][4 * c4 + 2] = __fmul_rn(x.z, g[4 * c4 + 2]);
+        t[pp][4 * c4 + 3] = __fmul_rn(x.w, g[4 * c4 + 3]);
       }
-      float mx = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        t[e] = __fmul_rn(t[e], g[e]);
-        mx = fmaxf(mx, fabsf(t[e]));
-      }
-      mx = max8(mx);
-      float sgm = 0.0f, hh = 0.0f;
-      if (mx != 0.0f) {
-        sgm = __fdiv_rn(mx, 127.0f);
-        hh = __fdiv_rn(127.0f, mx);
-      }
-      if (qq == 0) p.sigma[s * kD + i] = sgm;
+      for (int e = 0; e < 16; ++e) mx[pp] = fmaxf(mx[pp], fabsf(t[pp][e]));
+    }
+    // Row maxima over the lane group, shared out: lane (b0, b1, b2) ends with
+    // the maximum of its row pp = 2 b0 + b1 (max is exact in any order).
+    const bool b0 = (qq & 1) != 0, b1 = (qq & 2) != 0;
+    float m2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float keep = b0 ? mx[2 + k] : mx[k];
+      const float send = b0 ? mx[k] : mx[2 + k];
+      m2[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+    }
+    float m1 = fmaxf(b1 ? m2[1] : m2[0], __shfl_xor_sync(0xffffffffu, b1 ? m2[0] : m2[1], 2));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
+    // sigma = m / 127 and the reciprocal h = 127 / m, once per row; zero row: 0, 0.
+    float sgm = 0.0f, hown = 0.0f;
+    if (m1 != 0.0f) {
+      sgm = __fdiv_rn(m1, 127.0f);
+      hown = __fdiv_rn(127.0f, m1);
+    }
+    const int pp_own = 2 * (qq & 1) + ((qq >> 1) & 1);
+    if ((qq & 4) == 0) p.sigma[s * kD + 32 * pp_own + 4 * w + r] = sgm;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const float hh = __shfl_sync(0xffffffffu, hown, (lane & ~7) | ((pp >> 1) | ((pp & 1) << 1)));
+      const int i = 32 * pp + 4 * w + r;
       // Round t*h to the nearest integer, ties to even: |t*h| <= 127(1+2^-24)^2
       // < 127.5, so adding 1.5 * 2^23 leaves the integer, in [-127, 127], in
       // the low mantissa bits (two's complement), and no clamp is needed.
       uint32_t rb[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[e], hh), 12582912.0f));
+      for (int e = 0; e < 16; ++e) rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[pp][e], hh), 12582912.0f));
       uint32_t wd[4];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
@@ -1084,7 +1130,7 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, slots);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, false);
+  append_compute<KDA, 128, false>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
@@ -1102,11 +1148,12 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
-  append_compute<KDA, 256>(p, s, n, L, lq_dyn_smem, alpha_s, beta, n == p.W);
   if (n < p.W) {
+    append_compute<KDA, 256, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
+  append_compute<KDA, 256, true>(p, s, n, L, lq_dyn_smem, alpha_s, beta);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
