@@ -267,11 +267,11 @@ struct Tail {
   float* rowpart;  // [128][8]  per-row block partials of the squared length
   float* colpart;  // [8][128]  per-column block partials
   float* score;    // [256]     line scores: rows 0..127, columns 128..255
-  float* gsc_b;    // [160]     1 / lambda, blocked layout
+  float* gsc_b;    // [160]     1 / lambda, blocked layout (shares the score array)
   int* win;        // [4]
 };
 constexpr int kTileBytes = kD * kD * 4;
-constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + kBV + 4) * 4;
+constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + 4) * 4;
 
 __host__ __device__ inline int region1_bytes(const Stage& L) {
   const int r = L.end > kTileBytes ? L.end : kTileBytes;
@@ -286,9 +286,8 @@ __device__ __forceinline__ Tail carve_tail(char* base, int r1) {
   t.colpart = x;
   x += 8 * kD;
   t.score = x;
+  t.gsc_b = x;  // 1/lambda is written after the last read of the scores
   x += 256;
-  t.gsc_b = x;
-  x += kBV;
   t.win = reinterpret_cast<int*>(x);
   return t;
 }
@@ -439,10 +438,12 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       P[n] = pr;
       pr = __fmul_rn(pr, alpha_scalar);
       P[n - 1] = pr;
-#pragma unroll 4
-      for (int m = n - 1; m >= 1; --m) {
-        pr = __fmul_rn(pr, ra[m - 1]);
-        P[m - 1] = pr;
+#pragma unroll
+      for (int m = kMaxW - 1; m >= 1; --m) {
+        if (m <= n - 1) {
+          pr = __fmul_rn(pr, ra[m - 1]);
+          P[m - 1] = pr;
+        }
       }
     }
     __syncthreads();
@@ -671,6 +672,7 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
   const float* P_b = at<float>(sm, L.P_b);
   const float* rk = at<float>(sm, L.rec_k);
   float* kd_b = at<float>(sm, L.kd_b);
+#pragma unroll 4
   for (int e = tid; e < n * kD; e += 256) {
     const int m1 = e >> 7, j = e & (kD - 1);
     kd_b[m1 * kBV + bv(j)] = __fmul_rn(decay_at<KDA>(P, P_b, m1 + 1, j), rk[e]);
@@ -889,83 +891,98 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
 
-  // F2: C greedy rounds of the longest line, ties to the smallest id. Lane L
-  // scans ids L, L+32, ... in ascending order, then the warp keeps the larger
-  // score (the smaller id on a tie).
-  for (int c = 0; c < p.C; ++c) {
-    if (tid < 32) {
-      float bv_ = tl.score[tid];
-      int bi = tid;
+  // F2: C greedy rounds of the longest line, ties to the smallest id, run by
+  // warp 0 alone (no block barrier between rounds). Lane L scans ids L, L+32,
+  // ... in ascending order, then a butterfly keeps the larger score (the
+  // smaller id on a tie) in every lane. Taking a row refreshes the column
+  // partials of its row block (lane L: columns 4L..4L+3); taking a column
+  // refreshes the row partials of its column block (lane L: rows L + 32k).
+  if (w == 0) {
+    const int L = tid;
+    int qoff[8];  // chunk L of a row i with i & 7 == k sits at qoff[k]
+#pragma unroll
+    for (int k = 0; k < 8; ++k) qoff[k] = (L ^ ((((L >> 3) + k) & 3) | (k & 4))) << 2;
+    for (int c = 0; c < p.C; ++c) {
+      float bsc = tl.score[L];
+      int bi = L;
 #pragma unroll
       for (int e = 1; e < 8; ++e) {
-        const float v = tl.score[tid + 32 * e];
-        if (v > bv_) {
-          bv_ = v;
-          bi = tid + 32 * e;
+        const float v = tl.score[L + 32 * e];
+        if (v > bsc) {
+          bsc = v;
+          bi = L + 32 * e;
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_down_sync(0xffffffffu, bv_, off);
-        const int oi = __shfl_down_sync(0xffffffffu, bi, off);
-        if (ov > bv_ || (ov == bv_ && oi < bi)) {
-          bv_ = ov;
+        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bsc || (ov == bsc && oi < bi)) {
+          bsc = ov;
           bi = oi;
         }
       }
-      if (tid == 0) {
-        tl.win[0] = bi;
-        p.comp_id[s * p.comp_id_stride + c] = bi;
-      }
-    }
-    __syncthreads();
-    const int win = tl.win[0];
-    float* line = p.comp_line + (s * p.C + c) * kD;
-    if (win < kD) {
-      // Row win: copy, zero, refresh the column partials of its row block.
-      if (tid < kD) {
-        const int j = tid;
-        float* e = &S[win * kD + coff[win & 7]];
-        line[j] = *e;
-        *e = 0.0f;
+      const int win = bi;
+      if (L == 0) p.comp_id[s * p.comp_id_stride + c] = win;
+      float* line = p.comp_line + (s * p.C + c) * kD;
+      if (win < kD) {
+        // Row win: copy columns 4L..4L+3, zero them, then refresh block win/16.
+        float4* e = reinterpret_cast<float4*>(&S[win * kD + qoff[win & 7]]);
+        reinterpret_cast<float4*>(line)[L] = *e;
+        *e = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (L < 8) tl.rowpart[win * 8 + L] = 0.0f;
+        if (L == 0) tl.score[win] = 0.0f;
+        __syncwarp();
         const int b = win >> 4;
-        tl.colpart[b * kD + j] = column_block<true>(S, b, coff);
-        tl.score[kD + j] = tree8_mem(tl.colpart + j, kD);
-      } else if (tid < kD + 8) {
-        tl.rowpart[win * 8 + (tid - kD)] = 0.0f;
-      } else if (tid == kD + 8) {
-        tl.score[win] = 0.0f;
-      }
-    } else {
-      // Column js: copy, zero, refresh the row partials of its column block.
-      const int js = win - kD;
-      if (tid < kD) {
-        const int i = tid;
-        float* e = &S[sidx(i, js)];
-        line[i] = *e;
-        *e = 0.0f;
-        const int q = js >> 4;
-        int ro[4];
-        row_offsets(i, q, ro);
-        float pr = 0.0f;
+        const float* base = S + 16 * b * kD;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + ro[c4]]);
-          pr = __fmaf_rn(x.x, x.x, pr);
-          pr = __fmaf_rn(x.y, x.y, pr);
-          pr = __fmaf_rn(x.z, x.z, pr);
-          pr = __fmaf_rn(x.w, x.w, pr);
+        for (int t = 0; t < 16; ++t) {
+          const float4 x = *reinterpret_cast<const float4*>(base + t * kD + qoff[t & 7]);
+          a0 = __fmaf_rn(x.x, x.x, a0);
+          a1 = __fmaf_rn(x.y, x.y, a1);
+          a2 = __fmaf_rn(x.z, x.z, a2);
+          a3 = __fmaf_rn(x.w, x.w, a3);
         }
-        tl.rowpart[i * 8 + q] = pr;
-        tl.score[i] = tree8_mem(tl.rowpart + i * 8, 1);
-      } else if (tid < kD + 8) {
-        tl.colpart[(tid - kD) * kD + js] = 0.0f;
-      } else if (tid == kD + 8) {
-        tl.score[win] = 0.0f;
+        *reinterpret_cast<float4*>(tl.colpart + b * kD + 4 * L) = make_float4(a0, a1, a2, a3);
+        __syncwarp();
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) tl.score[kD + 4 * L + e4] = tree8_mem(tl.colpart + 4 * L + e4, kD);
+      } else {
+        // Column js: copy rows L + 32k, zero them, then refresh block js/16 of every row.
+        const int js = win - kD, cj = js >> 2, q = js >> 4;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = L + 32 * k;
+          float* e = &S[i * kD + (((cj ^ ((((cj >> 3) + i) & 3) | (i & 4))) << 2) + (js & 3))];
+          line[i] = *e;
+          *e = 0.0f;
+        }
+        if (L < 8) tl.colpart[L * kD + js] = 0.0f;
+        if (L == 0) tl.score[win] = 0.0f;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = L + 32 * k;
+          int ro[4];
+          row_offsets(i, q, ro);
+          float pr = 0.0f;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + ro[c4]]);
+            pr = __fmaf_rn(x.x, x.x, pr);
+            pr = __fmaf_rn(x.y, x.y, pr);
+            pr = __fmaf_rn(x.z, x.z, pr);
+            pr = __fmaf_rn(x.w, x.w, pr);
+          }
+          tl.rowpart[i * 8 + q] = pr;
+          tl.score[i] = tree8_mem(tl.rowpart + i * 8, 1);
+        }
       }
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // F3: smoothing scales from the residual's column sums of |R|.
   column_quads<false>(S, tl.colpart);
@@ -1136,7 +1153,7 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
 template <bool KDA>
-__global__ void __launch_bounds__(256, 2) k_step(Params p) {
+__global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -1167,7 +1184,7 @@ __global__ void __launch_bounds__(256, 2) k_step(Params p) {
 
 // Fold with the records held (any count 0..W): lq_fold.
 template <bool KDA>
-__global__ void __launch_bounds__(256, 2) k_fold(Params p) {
+__global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -1190,7 +1207,7 @@ __global__ void __launch_bounds__(256, 2) k_fold(Params p) {
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
 template <bool KDA>
-__global__ void __launch_bounds__(256, 2) k_export(Params p) {
+__global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -1217,7 +1234,7 @@ __global__ void __launch_bounds__(256, 2) k_export(Params p) {
 }
 
 // Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
-__global__ void __launch_bounds__(256, 2) k_init(Params p) {
+__global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1261,6 +1278,8 @@ static int smem_of(const Params& q, bool tile) { return tile ? q.r1 + kTailBytes
 template <typename K>
 static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, int threads = 256) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   kernel<<<dim3((unsigned)p.n_states), dim3(threads), (size_t)smem, st>>>(p);
   return cudaGetLastError();
