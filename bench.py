@@ -43,7 +43,7 @@ if ROOT not in sys.path:
 METRIC = "head-tokens/s and achieved HBM GB/s (% of GB300 peak) at batch 32/128/512"
 UNIT = "head-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_append_gdn_batch512.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_append_gdn_batch128.md")
 KERNEL_SOURCE = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc", "lq_kernels.cu")
 
 
@@ -116,9 +116,11 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def profile_traffic():
-    """(bytes per launch, note) from the committed ncu summary of the dominant kernel,
-    or (None, why) when there is none or the kernel source changed since it was taken."""
+def profile_traffic(n_states):
+    """(DRAM bytes per launch at n_states, note) from the committed ncu summary of the
+    dominant kernel, scaled from the captured head-states (traffic grows in
+    proportion to them), or (None, why) when there is none or the kernel source
+    changed since it was taken."""
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
@@ -132,9 +134,11 @@ def profile_traffic():
     if fields.get("kernel_source_sha256") != src:
         return None, "kernel changed since the ncu capture"
     try:
-        return float(fields["dram_bytes_per_launch"]), "ncu capture"
+        per = float(fields["dram_bytes_per_launch"])
+        cap = int(fields["captured_head_states"])
     except (KeyError, ValueError):
-        return None, "summary lacks dram_bytes_per_launch"
+        return None, "summary lacks dram_bytes_per_launch / captured_head_states"
+    return round(per * n_states / cap), f"ncu capture at {cap} head-states, phase-averaged, scaled to {n_states}"
 
 
 class ClockSampler:
@@ -440,7 +444,7 @@ def run_ours(args):
     app_ms = statistics.mean(app)
     fold_ms = statistics.mean(fold)
     achieved = app_bytes / (app_ms / 1e3) / 1e9
-    traffic, traffic_note = profile_traffic()
+    traffic, traffic_note = profile_traffic(N)
     fold_bytes = N * (alg_bytes_append(W - 1, wl.C, wl.kda) + alg_bytes_fold_extra(wl.C))
     win_bytes = N * alg_bytes_window(W, wl.C, wl.kda)
     win_gbs = win_bytes / (t_ms / K / 1e3) / 1e9
