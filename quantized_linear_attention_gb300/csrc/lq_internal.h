@@ -32,9 +32,9 @@ static_assert(sizeof(Header) == 256, "header is 256 bytes");
 // (computed on the host for the kernel being launched).
 struct Stage {
   // staged by bulk copies, dense
-  int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, q, k, v, alpha_cur;
+  int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha;
   // computed, blocked layout
-  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, line_b, lam_b, kd_b, bd_b, P_b;
+  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, lam_b, kd_b, bd_b, P_b;
   // computed, dense
   int basek, baseq, P, g, h, ec, eq, ca;
   int end;

@@ -214,8 +214,9 @@ __host__ __device__ __forceinline__ int bv(int j) { return j + ((j >> 4) << 2); 
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
-// slots_u: staged record slots of u and alpha; slots_k: staged slots of k (the
-// fold reads every record key; the append reads keys straight into registers).
+// slots_u: staged record slots of u and alpha; slots_k: staged slots of k (0
+// when the keys travel in registers). The token's q, k, v (and alpha) are read
+// into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
                                               bool append, bool fold) {
   Stage L;
@@ -234,17 +235,12 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.rec_k = take(4 * kD * slots_k);
   L.rec_u = take(4 * kD * slots_u);
   L.rec_alpha = take(kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
-  L.q = take(va * 4 * kD);
-  L.k = take(va * 4 * kD);
-  L.v = take(va * 4 * kD);
-  L.alpha_cur = take(va * kda * 4 * kD);
   L.kn_b = take(va * 4 * kBV);
   L.qn_b = take(va * 4 * kBV);
   L.y_b = take(va * 4 * kBV);
   L.aq_b = take(va * 4 * kBV);
   L.zk_b = take(va * 4 * kBV);
   L.zq_b = take(va * 4 * kBV);
-  L.line_b = take(0);
   L.lam_b = take(fo * 4 * kBV);
   L.kd_b = take(fo * 4 * kBV * W);
   L.bd_b = take(fo * 4 * kBV * C);
@@ -305,12 +301,12 @@ namespace lqi {
 // Staging: one thread issues every copy of head-state s (n0 records held) on
 // `bar`, with the exact byte count announced first.
 __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, const Stage& L, char* sm,
-                                            uint64_t* bar, bool append, bool stage_k) {
+                                            uint64_t* bar, bool stage_k) {
   const uint32_t rec = 4u * kD * (uint32_t)n0;
   const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
-  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec + alpha_bytes;
+  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec;
+  if (!p.kda || n0 > 0) bytes += alpha_bytes;
   if (stage_k) bytes += rec;
-  if (append) bytes += 12u * kD + (p.kda ? 4u * kD : 0u);
   mbar_expect_tx(bar, bytes);
   bulk_g2s(sm + L.codes, p.codes + s * (kD * kD), kD * kD, bar);
   bulk_g2s(sm + L.sigma, p.sigma + s * kD, 4 * kD, bar);
@@ -322,12 +318,6 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
     bulk_g2s(sm + L.rec_u, p.rec_u + s * p.W * kD, rec, bar);
   }
   if (!p.kda || n0 > 0) bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
-  if (append) {
-    bulk_g2s(sm + L.q, p.q + s * kD, 4 * kD, bar);
-    bulk_g2s(sm + L.k, p.k + s * kD, 4 * kD, bar);
-    bulk_g2s(sm + L.v, p.v + s * kD, 4 * kD, bar);
-    if (p.kda) bulk_g2s(sm + L.alpha_cur, p.alpha + s * kD, 4 * kD, bar);
-  }
 }
 
 // Decay products from staged alphas (records 1..n-1, then alpha_n = the current
@@ -387,9 +377,32 @@ __device__ __forceinline__ float decay_at(const float* P, const float* P_b, int 
 // With FOLD (the window fills), the new record is also left in the staged buffers.
 // NT threads (128 or 256); lane group (w, r) owns rows pp * 4 * (NT/32) + 4w + r,
 // lane qq owns the 16-element block qq of every vector.
-template <bool KDA, int NT, bool FOLD>
+
+// The token's inputs as thread t < 128 holds them: q[t], k[t] and (KDA)
+// alpha[t] for key channel t, v[t] for value row t.
+struct TokenRegs {
+  float q, k, v, a;
+};
+
+__device__ __forceinline__ TokenRegs load_token(const Params& p, int64_t s) {
+  TokenRegs t{0.0f, 0.0f, 0.0f, 0.0f};
+  const int j = threadIdx.x;
+  if (j < kD) {
+    t.q = p.q[s * kD + j];
+    t.k = p.k[s * kD + j];
+    t.v = p.v[s * kD + j];
+    if (p.kda) t.a = p.alpha[s * kD + j];
+  }
+  return t;
+}
+
+// KPRE: record keys are not staged; lane group g arrives with block qq of
+// record slot g in `kpre` (read before the staging wait), and slots beyond the
+// first round of lane groups are read from global memory.
+template <bool KDA, int NT, bool FOLD, bool KPRE>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
-                                               float alpha_scalar, float beta) {
+                                               float alpha_scalar, float beta, const TokenRegs& tk,
+                                               const float4 (&kpre)[4]) {
   constexpr int NW = NT / 32;
   constexpr int RPT = 128 / (4 * NW);  // rows per thread: 8 or 4
   constexpr int NG = NT / 8;           // lane groups
@@ -397,8 +410,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   float* P = at<float>(sm, L.P);
   float* P_b = at<float>(sm, L.P_b);
-  const float* kn = at<float>(sm, L.k);
-  const float* qn = at<float>(sm, L.q);
   float* kn_b = at<float>(sm, L.kn_b);
   float* qn_b = at<float>(sm, L.qn_b);
   float* y_b = at<float>(sm, L.y_b);
@@ -423,17 +434,29 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // the scalar chain into the table.
   if (KDA) {
     if (tid < kD) {
-      const float* ac = at<float>(sm, L.alpha_cur);
       const int jb = bv(tid);
       float pr = 1.0f;
       P_b[n * kBV + jb] = pr;
       for (int m = n; m >= 1; --m) {
-        pr = __fmul_rn(pr, m == n ? ac[tid] : ra[(m - 1) * kD + tid]);
+        pr = __fmul_rn(pr, m == n ? tk.a : ra[(m - 1) * kD + tid]);
         P_b[(m - 1) * kBV + jb] = pr;
       }
     }
   } else {
     if (tid == 0) {
+      // Every staged alpha is read before the first product is stored, so the
+      // chain runs at multiply latency rather than load latency.
+      float al[kMaxW];
+#pragma unroll
+      for (int q4 = 0; q4 < kMaxW / 4; ++q4) {
+        if (4 * q4 < n - 1) {
+          const float4 a4 = *reinterpret_cast<const float4*>(ra + 4 * q4);
+          al[4 * q4] = a4.x;
+          al[4 * q4 + 1] = a4.y;
+          al[4 * q4 + 2] = a4.z;
+          al[4 * q4 + 3] = a4.w;
+        }
+      }
       float pr = 1.0f;
       P[n] = pr;
       pr = __fmul_rn(pr, alpha_scalar);
@@ -441,7 +464,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
 #pragma unroll
       for (int m = kMaxW - 1; m >= 1; --m) {
         if (m <= n - 1) {
-          pr = __fmul_rn(pr, ra[m - 1]);
+          pr = __fmul_rn(pr, al[m - 1]);
           P[m - 1] = pr;
         }
       }
@@ -452,11 +475,10 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   if (tid < kD) {
     const int j = tid, jb = bv(j);
     const float A = KDA ? P_b[jb] : P[0];
-    const float kj = kn[j], qj = qn[j];
-    const float yy = __fmul_rn(A, kj);
-    const float qa = __fmul_rn(A, qj);
-    kn_b[jb] = kj;
-    qn_b[jb] = qj;
+    const float yy = __fmul_rn(A, tk.k);
+    const float qa = __fmul_rn(A, tk.q);
+    kn_b[jb] = tk.k;
+    qn_b[jb] = tk.q;
     y_b[jb] = yy;
     aq_b[jb] = qa;
     zk_b[jb] = __fmul_rn(lam[j], yy);
@@ -477,14 +499,23 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       if (job < njobs) {
         if (job < nrec) {
           const int m = job + 1;
-          const float4* kv4 = reinterpret_cast<const float4*>(at<float>(sm, L.rec_k) + (m - 1) * kD + 16 * qq);
+          float4 kv[4];
+          if (KPRE && base == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = kpre[c4];
+          } else {
+            const float4* src = KPRE ? reinterpret_cast<const float4*>(p.rec_k + (s * p.W + job) * kD + 16 * qq)
+                                     : reinterpret_cast<const float4*>(at<float>(sm, L.rec_k) + job * kD + 16 * qq);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = src[c4];
+          }
           const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
           const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
           const float4* pm4 = reinterpret_cast<const float4*>(P_b + m * kBV + 20 * qq);
           const float pms = KDA ? 0.0f : P[m];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 kvc = kv4[c4], kx = kx4[c4], qx = qx4[c4];
+            const float4 kvc = kv[c4], kx = kx4[c4], qx = qx4[c4];
             const float kvs[4] = {kvc.x, kvc.y, kvc.z, kvc.w};
             const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
             if (KDA) {
@@ -609,22 +640,24 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // u_n = beta (v - acc). A6: the output in any order. A7: store record n.
   // A row compensator's coefficient a_c[i] is zero except on its own row, and
   // fma(0, x, acc) returns acc for the finite, never negative-zero acc here.
-  float* ru = at<float>(sm, L.rec_u);
-  const float* vv = at<float>(sm, L.v);
-  const int64_t rec_off = (s * p.W + (n - 1)) * kD;  // record slot n-1 of head-state s
   if (tid < kD) {
     const int i = tid;
+    float* ru = at<float>(sm, L.rec_u);
+    const int64_t rec_off = (s * p.W + (n - 1)) * kD;  // record slot n-1 of head-state s
     float acc = basek[i];
     float oo = baseq[i];
-    for (int c = 0; c < p.C; ++c) {
-      const int id = cid[c];
-      if (id >= kD) {
-        const float a = cl[c * kD + i];
-        acc = __fmaf_rn(a, ec[c], acc);
-        oo = __fmaf_rn(a, eq[c], oo);
-      } else if (id == i) {
-        acc = __fmaf_rn(1.0f, ec[c], acc);
-        oo = __fmaf_rn(1.0f, eq[c], oo);
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      if (c < p.C) {
+        const int id = cid[c];
+        if (id >= kD) {
+          const float a = cl[c * kD + i];
+          acc = __fmaf_rn(a, ec[c], acc);
+          oo = __fmaf_rn(a, eq[c], oo);
+        } else if (id == i) {
+          acc = __fmaf_rn(1.0f, ec[c], acc);
+          oo = __fmaf_rn(1.0f, eq[c], oo);
+        }
       }
     }
     const float* rui = ru + i;
@@ -634,20 +667,19 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       acc = __fmaf_rn(um, g[m], acc);
       oo = __fmaf_rn(um, h[m], oo);
     }
-    const float u = __fmul_rn(beta, __fsub_rn(vv[i], acc));
+    const float u = __fmul_rn(beta, __fsub_rn(tk.v, acc));
     oo = __fmaf_rn(u, h[n], oo);
     p.rec_u[rec_off + i] = u;
     p.o[s * kD + i] = oo;
-    if (FOLD) ru[(n - 1) * kD + i] = u;
-  }
-  if (NT == kD || tid >= kD) {
-    const int j = NT == kD ? tid : tid - kD;
-    p.rec_k[rec_off + j] = kn[j];
-    if (FOLD) at<float>(sm, L.rec_k)[(n - 1) * kD + j] = kn[j];
+    p.rec_k[rec_off + i] = tk.k;
     if (KDA)
-      p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + j] = at<float>(sm, L.alpha_cur)[j];
-    else if (j == 0)
+      p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + i] = tk.a;
+    else if (i == 0)
       p.rec_alpha[s * p.alpha_stride + (n - 1)] = alpha_scalar;
+    if (FOLD) {
+      ru[(n - 1) * kD + i] = u;
+      at<float>(sm, L.rec_k)[(n - 1) * kD + i] = tk.k;
+    }
   }
 }
 
@@ -1080,17 +1112,16 @@ struct StageInfo {
 };
 
 __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int known_n0, const Stage& L,
-                                                 uint64_t* bar, StageInfo* sh, bool append, bool stage_k,
-                                                 int max_n0) {
+                                                 uint64_t* bar, StageInfo* sh, bool stage_k, int max_n0) {
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     int n0 = known_n0;
-    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append, stage_k);
+    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k);
     const int c = p.counts[s];
     const int h = header_ok(p) ? 1 : 0;
     if (n0 < 0) {
       n0 = (h && c >= 0 && c <= max_n0) ? c : -1;
-      if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, append, stage_k);
+      if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k);
     }
     sh->issued = n0;
     sh->cnt = c;
@@ -1134,7 +1165,9 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
 // lq_append. With a stated phase the staging area holds exactly `phase` records.
 __host__ __device__ inline int append_slots(int W, int phase) { return (phase >= 0 && phase < W) ? phase : W - 1; }
 
-template <bool KDA>
+// KPRE (the phase is stated): the record keys are not staged; each lane group
+// reads its record's key block into registers before the staging wait.
+template <bool KDA, bool KPRE>
 __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1144,10 +1177,20 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, slots);
+  const TokenRegs tk = load_token(p, s);
+  float4 kpre[4];
+  if (KPRE) {
+    const int grp = threadIdx.x >> 3, qq = threadIdx.x & 7;
+    if (grp < known) {
+      const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * p.W + grp) * kD + 16 * qq);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) kpre[c4] = src[c4];
+    }
+  }
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, !KPRE, slots);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta);
+  append_compute<KDA, 128, false, KPRE>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
@@ -1161,16 +1204,18 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   const float beta = p.beta[s];
   const float alpha_s = KDA ? 0.0f : p.alpha[s];
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, true, p.W - 1);
+  const TokenRegs tk = load_token(p, s);
+  float4 kpre[4];
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, p.W - 1);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
   if (n < p.W) {
-    append_compute<KDA, 256, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta);
+    append_compute<KDA, 256, false, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  append_compute<KDA, 256, true>(p, s, n, L, lq_dyn_smem, alpha_s, beta);
+  append_compute<KDA, 256, true, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
@@ -1189,7 +1234,7 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
   const Stage& L = p.st;
-  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, false, true, p.W);
+  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, true, p.W);
   const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
@@ -1214,7 +1259,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   const Stage& L = p.st;
-  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, false, true, p.W);
+  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, true, p.W);
   const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
@@ -1292,9 +1337,12 @@ cudaError_t launch_init(const Params& p, cudaStream_t st) {
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const int slots = append_slots(p.W, p.phase);
-  const Params q = with_layout(p, slots, slots, true, false, false);
-  return p.kda ? launch(k_append<true>, q, smem_of(q, false), st, 128)
-               : launch(k_append<false>, q, smem_of(q, false), st, 128);
+  const bool stated = p.phase >= 0 && p.phase < p.W;
+  const Params q = with_layout(p, slots, stated ? 0 : slots, true, false, false);
+  const int smem = smem_of(q, false);
+  if (stated)
+    return p.kda ? launch(k_append<true, true>, q, smem, st, 128) : launch(k_append<false, true>, q, smem, st, 128);
+  return p.kda ? launch(k_append<true, false>, q, smem, st, 128) : launch(k_append<false, false>, q, smem, st, 128);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
