@@ -58,6 +58,48 @@ __device__ __forceinline__ float code_f(uint32_t biased_word, int b) {
   return __fsub_rn(__uint_as_float(bits), 8388736.0f);
 }
 
+// Packed fp32 pairs (the .f32x2 forms of mul / fma): each half is the
+// round-to-nearest IEEE result of its own lane, subnormals kept, so one pair
+// instruction is exactly two scalar operations issued at once.
+typedef unsigned long long f32x2;  // low half = first element
+
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_bits(uint32_t lo, uint32_t hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Exact int8 -> fp32 of bytes b and b' of two biased words, as one pair.
+__device__ __forceinline__ f32x2 code_pair(uint32_t w_lo, int b_lo, uint32_t w_hi, int b_hi) {
+  const f32x2 bias = f2_pack(8388736.0f, 8388736.0f);
+  return f2_sub(f2_bits(__byte_perm(w_lo, 0x4B000000u, 0x7540u | (uint32_t)b_lo),
+                        __byte_perm(w_hi, 0x4B000000u, 0x7540u | (uint32_t)b_hi)),
+                bias);
+}
+
 __device__ __forceinline__ void codes16_to_float(int4 c, float f[16]) {
   const uint32_t w[4] = {(uint32_t)c.x ^ 0x80808080u, (uint32_t)c.y ^ 0x80808080u, (uint32_t)c.z ^ 0x80808080u,
                          (uint32_t)c.w ^ 0x80808080u};
@@ -263,11 +305,11 @@ struct Tail {
   float* rowpart;  // [128][8]  per-row block partials of the squared length
   float* colpart;  // [8][128]  per-column block partials
   float* score;    // [256]     line scores: rows 0..127, columns 128..255
+  float* score2;   // [256]     the next round's scores (selection rounds alternate)
   float* gsc_b;    // [160]     1 / lambda, blocked layout (shares the score array)
-  int* win;        // [4]
 };
 constexpr int kTileBytes = kD * kD * 4;
-constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + 4) * 4;
+constexpr int kTailBytes = (8 * kD + 8 * kD + 256 + 256) * 4;
 
 __host__ __device__ inline int region1_bytes(const Stage& L) {
   const int r = L.end > kTileBytes ? L.end : kTileBytes;
@@ -284,7 +326,7 @@ __device__ __forceinline__ Tail carve_tail(char* base, int r1) {
   t.score = x;
   t.gsc_b = x;  // 1/lambda is written after the last read of the scores
   x += 256;
-  t.win = reinterpret_cast<int*>(x);
+  t.score2 = x;
   return t;
 }
 
@@ -728,7 +770,7 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
 
 // F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
 // lambda_j) P_0[j], then the compensators in order, then the records in order,
-// each an fma.
+// each an fma. Adjacent columns (2k, 2k+1) of a row travel as one packed pair.
 template <bool KDA>
 __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
@@ -739,46 +781,49 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   const float* bd_b = at<float>(sm, L.bd_b);
   const float* kd_b = at<float>(sm, L.kd_b);
   const float* U = at<float>(sm, L.rec_u);
+  f32x2 a2[4][8];
   {
-    float lam[16], p0[16];
-    load16(at<float>(sm, L.lam_b) + 20 * qq, lam);
-    decay_block<KDA>(P, P_b, 0, qq, p0);
+    // lambda and P_0 pairs are read per row (8-byte loads) to keep registers
+    // for the 32 accumulator pairs.
+    const f32x2* lam2 = reinterpret_cast<const f32x2*>(at<float>(sm, L.lam_b) + 20 * qq);
+    const f32x2* p02 = reinterpret_cast<const f32x2*>(P_b + 20 * qq);
+    const f32x2 p0s = f2_pack(P[0], P[0]);
     const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
-      const float s_i = sg[i];
-      float f[16];
-      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
+      const f32x2 s2 = f2_pack(sg[i], sg[i]);
+      const int4 c = *reinterpret_cast<const int4*>(cb + i * kD);
+      const uint32_t cw[4] = {(uint32_t)c.x ^ 0x80808080u, (uint32_t)c.y ^ 0x80808080u, (uint32_t)c.z ^ 0x80808080u,
+                              (uint32_t)c.w ^ 0x80808080u};
 #pragma unroll
-      for (int t = 0; t < 16; ++t) acc[pp][t] = __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[t]), lam[t]), p0[t]);
+      for (int k = 0; k < 8; ++k) {
+        const f32x2 f = code_pair(cw[k >> 1], (2 * k) & 3, cw[k >> 1], (2 * k + 1) & 3);
+        a2[pp][k] = f2_mul(f2_mul(f2_mul(s2, f), lam2[k]), KDA ? p02[k] : p0s);
+      }
     }
   }
   // Compensators in order. The term fma(a_c[i], (P_0 . b_c)[j], S_ij) has a
   // zero coefficient everywhere except on the compensator's own line, and there
   // it returns S_ij unchanged (S is finite and never negative zero here), so
   // only that line is touched: a row compensator adds P_0 . line to its row, a
-  // column compensator j0 adds line[i] * P_0[j0] to column j0.
+  // column compensator j0 adds line[i] * P_0[j0] to column j0 (as a pair whose
+  // other half is fma(0, 0, S) = S).
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
+  const f32x2 one2 = f2_pack(1.0f, 1.0f);
   for (int c = 0; c < p.C; ++c) {
     const int id = cid[c];
     if (id < kD) {
       if (((id & 31) >> 2) == w) {  // warp-uniform: row id is one of this warp's rows
         const int pp_own = id >> 5;
         if ((id & 3) == r) {
-          const float4* b4 = reinterpret_cast<const float4*>(bd_b + c * kBV + 20 * qq);
+          const f32x2* b2 = reinterpret_cast<const f32x2*>(bd_b + c * kBV + 20 * qq);
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
             if (pp != pp_own) continue;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              const float4 b = b4[c4];
-              acc[pp][4 * c4 + 0] = __fmaf_rn(1.0f, b.x, acc[pp][4 * c4 + 0]);
-              acc[pp][4 * c4 + 1] = __fmaf_rn(1.0f, b.y, acc[pp][4 * c4 + 1]);
-              acc[pp][4 * c4 + 2] = __fmaf_rn(1.0f, b.z, acc[pp][4 * c4 + 2]);
-              acc[pp][4 * c4 + 3] = __fmaf_rn(1.0f, b.w, acc[pp][4 * c4 + 3]);
-            }
+            for (int k = 0; k < 8; ++k) a2[pp][k] = f2_fma(one2, b2[k], a2[pp][k]);
           }
         }
       }
@@ -786,20 +831,24 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
       const int j0 = id - kD;
       if (qq == (j0 >> 4)) {
         const float pj = KDA ? P_b[bv(j0)] : P[0];
-        float li[4];
+        const bool odd = (j0 & 1) != 0;
+        const f32x2 pj2 = odd ? f2_pack(0.0f, pj) : f2_pack(pj, 0.0f);
+        f32x2 li2[4];
 #pragma unroll
-        for (int pp = 0; pp < 4; ++pp) li[pp] = cl[c * kD + 32 * pp + 4 * w + r];
-        switch (j0 & 15) {
-#define LQ_COLCOMP(T)                                                                   \
-  case T:                                                                              \
-    acc[0][T] = __fmaf_rn(li[0], pj, acc[0][T]);                                       \
-    acc[1][T] = __fmaf_rn(li[1], pj, acc[1][T]);                                       \
-    acc[2][T] = __fmaf_rn(li[2], pj, acc[2][T]);                                       \
-    acc[3][T] = __fmaf_rn(li[3], pj, acc[3][T]);                                       \
+        for (int pp = 0; pp < 4; ++pp) {
+          const float li = cl[c * kD + 32 * pp + 4 * w + r];
+          li2[pp] = odd ? f2_pack(0.0f, li) : f2_pack(li, 0.0f);
+        }
+        switch ((j0 & 15) >> 1) {
+#define LQ_COLCOMP(K)                          \
+  case K:                                      \
+    a2[0][K] = f2_fma(li2[0], pj2, a2[0][K]);  \
+    a2[1][K] = f2_fma(li2[1], pj2, a2[1][K]);  \
+    a2[2][K] = f2_fma(li2[2], pj2, a2[2][K]);  \
+    a2[3][K] = f2_fma(li2[3], pj2, a2[3][K]);  \
     break;
           LQ_COLCOMP(0) LQ_COLCOMP(1) LQ_COLCOMP(2) LQ_COLCOMP(3) LQ_COLCOMP(4) LQ_COLCOMP(5) LQ_COLCOMP(6)
-          LQ_COLCOMP(7) LQ_COLCOMP(8) LQ_COLCOMP(9) LQ_COLCOMP(10) LQ_COLCOMP(11) LQ_COLCOMP(12)
-          LQ_COLCOMP(13) LQ_COLCOMP(14) LQ_COLCOMP(15)
+          LQ_COLCOMP(7)
 #undef LQ_COLCOMP
           default:
             break;
@@ -807,23 +856,27 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
       }
     }
   }
+  // Records in order; one row at a time, so that only one (u, u) pair and one
+  // key quad are live beside the 32 accumulator pairs.
+#pragma unroll 1
   for (int m = 0; m < n; ++m) {
-    float u[4];
+    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kd_b + m * kBV + 20 * qq);
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) u[pp] = U[m * kD + 32 * pp + 4 * w + r];
-    const float4* k4 = reinterpret_cast<const float4*>(kd_b + m * kBV + 20 * qq);
+    for (int pp = 0; pp < 4; ++pp) {
+      const float u = U[m * kD + 32 * pp + 4 * w + r];
+      const f32x2 u2 = f2_pack(u, u);
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const float4 b = k4[c4];
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        acc[pp][4 * c4 + 0] = __fmaf_rn(u[pp], b.x, acc[pp][4 * c4 + 0]);
-        acc[pp][4 * c4 + 1] = __fmaf_rn(u[pp], b.y, acc[pp][4 * c4 + 1]);
-        acc[pp][4 * c4 + 2] = __fmaf_rn(u[pp], b.z, acc[pp][4 * c4 + 2]);
-        acc[pp][4 * c4 + 3] = __fmaf_rn(u[pp], b.w, acc[pp][4 * c4 + 3]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const ulonglong2 b = k4[c4];
+        a2[pp][2 * c4] = f2_fma(u2, b.x, a2[pp][2 * c4]);
+        a2[pp][2 * c4 + 1] = f2_fma(u2, b.y, a2[pp][2 * c4 + 1]);
       }
     }
   }
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f2_unpack(a2[pp][k], acc[pp][2 * k], acc[pp][2 * k + 1]);
 }
 
 // Offsets of the four 16-byte chunks of block qq within row i of the tile
@@ -923,98 +976,101 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
 
-  // F2: C greedy rounds of the longest line, ties to the smallest id, run by
-  // warp 0 alone (no block barrier between rounds). Lane L scans ids L, L+32,
-  // ... in ascending order, then a butterfly keeps the larger score (the
-  // smaller id on a tie) in every lane. Taking a row refreshes the column
-  // partials of its row block (lane L: columns 4L..4L+3); taking a column
-  // refreshes the row partials of its column block (lane L: rows L + 32k).
-  if (w == 0) {
-    const int L = tid;
-    int qoff[8];  // chunk L of a row i with i & 7 == k sits at qoff[k]
+  // F2: C greedy rounds of the longest line, ties to the smallest id. Every
+  // warp finds the winner itself from this round's scores (lane L scans ids L,
+  // L+32, ... in ascending order, then a butterfly keeps the larger score, the
+  // smaller id on a tie). The next round's scores go to the other score array,
+  // so nothing a round reads is written during it. Then, in parallel:
+  //  - threads 0..127 refresh the scores the taken line changes: taking row i*
+  //    changes the block i*/16 partial of every column; taking column j*
+  //    changes the block j*/16 partial of every row. The refresh skips the
+  //    taken line's entries: they are zero in the residual, and fma(0, 0, acc)
+  //    = acc for the non-negative chains here;
+  //  - threads 128..255 carry the unchanged scores over (the taken line's
+  //    becomes 0), copy the line out exactly, zero it in the tile and clear its
+  //    partials.
+  // One barrier ends each round.
+  for (int c = 0; c < p.C; ++c) {
+    const float* cur = (c & 1) ? tl.score2 : tl.score;
+    float* nxt = (c & 1) ? tl.score : tl.score2;
+    const int L = tid & 31;
+    float bsc = cur[L];
+    int bi = L;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) qoff[k] = (L ^ ((((L >> 3) + k) & 3) | (k & 4))) << 2;
-    for (int c = 0; c < p.C; ++c) {
-      float bsc = tl.score[L];
-      int bi = L;
-#pragma unroll
-      for (int e = 1; e < 8; ++e) {
-        const float v = tl.score[L + 32 * e];
-        if (v > bsc) {
-          bsc = v;
-          bi = L + 32 * e;
-        }
+    for (int e = 1; e < 8; ++e) {
+      const float v = cur[L + 32 * e];
+      if (v > bsc) {
+        bsc = v;
+        bi = L + 32 * e;
       }
+    }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bsc || (ov == bsc && oi < bi)) {
-          bsc = ov;
-          bi = oi;
-        }
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bsc || (ov == bsc && oi < bi)) {
+        bsc = ov;
+        bi = oi;
       }
-      const int win = bi;
-      if (L == 0) p.comp_id[s * p.comp_id_stride + c] = win;
-      float* line = p.comp_line + (s * p.C + c) * kD;
-      if (win < kD) {
-        // Row win: copy columns 4L..4L+3, zero them, then refresh block win/16.
-        float4* e = reinterpret_cast<float4*>(&S[win * kD + qoff[win & 7]]);
-        reinterpret_cast<float4*>(line)[L] = *e;
-        *e = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (L < 8) tl.rowpart[win * 8 + L] = 0.0f;
-        if (L == 0) tl.score[win] = 0.0f;
-        __syncwarp();
-        const int b = win >> 4;
+    }
+    const int win = bi;
+    float* line = p.comp_line + (s * p.C + c) * kD;
+    if (win < kD) {
+      const int b = win >> 4;
+      if (tid < kD) {
+        // column j = tid: block-b chain over rows 16b..16b+15 without row win
         const float* base = S + 16 * b * kD;
-        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        float acc = 0.0f;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const float4 x = *reinterpret_cast<const float4*>(base + t * kD + qoff[t & 7]);
-          a0 = __fmaf_rn(x.x, x.x, a0);
-          a1 = __fmaf_rn(x.y, x.y, a1);
-          a2 = __fmaf_rn(x.z, x.z, a2);
-          a3 = __fmaf_rn(x.w, x.w, a3);
+          const float x = base[t * kD + coff[t & 7]];
+          if (16 * b + t != win) acc = __fmaf_rn(x, x, acc);
         }
-        *reinterpret_cast<float4*>(tl.colpart + b * kD + 4 * L) = make_float4(a0, a1, a2, a3);
-        __syncwarp();
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) tl.score[kD + 4 * L + e4] = tree8_mem(tl.colpart + 4 * L + e4, kD);
+        tl.colpart[b * kD + tid] = acc;
+        nxt[kD + tid] = tree8_mem(tl.colpart + tid, kD);
       } else {
-        // Column js: copy rows L + 32k, zero them, then refresh block js/16 of every row.
-        const int js = win - kD, cj = js >> 2, q = js >> 4;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = L + 32 * k;
-          float* e = &S[i * kD + (((cj ^ ((((cj >> 3) + i) & 3) | (i & 4))) << 2) + (js & 3))];
-          line[i] = *e;
-          *e = 0.0f;
-        }
-        if (L < 8) tl.colpart[L * kD + js] = 0.0f;
-        if (L == 0) tl.score[win] = 0.0f;
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = L + 32 * k;
-          int ro[4];
-          row_offsets(i, q, ro);
-          float pr = 0.0f;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + ro[c4]]);
-            pr = __fmaf_rn(x.x, x.x, pr);
-            pr = __fmaf_rn(x.y, x.y, pr);
-            pr = __fmaf_rn(x.z, x.z, pr);
-            pr = __fmaf_rn(x.w, x.w, pr);
-          }
-          tl.rowpart[i * 8 + q] = pr;
-          tl.score[i] = tree8_mem(tl.rowpart + i * 8, 1);
+        const int t2 = tid - kD;  // row t2's score carries over
+        nxt[t2] = t2 == win ? 0.0f : cur[t2];
+        if (t2 < 32) {
+          float4* e = reinterpret_cast<float4*>(&S[win * kD + ((t2 ^ ((((t2 >> 3) + win) & 3) | (win & 4))) << 2)]);
+          reinterpret_cast<float4*>(line)[t2] = *e;
+          *e = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else if (t2 < 40) {
+          tl.rowpart[win * 8 + (t2 - 32)] = 0.0f;
+        } else if (t2 == 40) {
+          p.comp_id[s * p.comp_id_stride + c] = win;
         }
       }
-      __syncwarp();
+    } else {
+      const int js = win - kD, q = js >> 4;
+      if (tid < kD) {
+        // row i = tid: block-q chain over columns 16q..16q+15 without column js
+        const int i = tid;
+        int ro[4];
+        row_offsets(i, q, ro);
+        float acc = 0.0f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + ro[c4]]);
+          const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (16 * q + 4 * c4 + e != js) acc = __fmaf_rn(xs[e], xs[e], acc);
+        }
+        tl.rowpart[i * 8 + q] = acc;
+        nxt[i] = tree8_mem(tl.rowpart + i * 8, 1);
+      } else {
+        const int i = tid - kD;  // column i's score carries over
+        nxt[kD + i] = kD + i == win ? 0.0f : cur[kD + i];
+        float* e = &S[sidx(i, js)];
+        line[i] = *e;
+        *e = 0.0f;
+        if (i < 8) tl.colpart[i * kD + js] = 0.0f;
+        if (i == 8) p.comp_id[s * p.comp_id_stride + c] = win;
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   // F3: smoothing scales from the residual's column sums of |R|.
   column_quads<false>(S, tl.colpart);
