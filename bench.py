@@ -65,6 +65,12 @@ def alg_bytes_fold_extra(C=4, D=128):
     return D * D + 4 * D + 4 * D + 4 * C + 4 * C * D
 
 
+def alg_bytes_fp32(kda=False, D=128):
+    """Per head-token of the fp32-state baseline: the whole state read and written,
+    the token's inputs read, o written."""
+    return 2 * 4 * D * D + 4 * D * 3 + 4 * (D if kda else 1) + 4 + 4 * D
+
+
 def alg_bytes_window(W=16, C=4, kda=False):
     """Per head-state per window: W-1 appends and one fused append+fold."""
     return sum(alg_bytes_append(p, C, kda) for p in range(W)) + alg_bytes_fold_extra(C)
@@ -346,6 +352,43 @@ def time_graphed(wl, steps, device):
     return total, app, fold
 
 
+def time_fp32(wl, device, tokens=48, warmup=4):
+    """The fp32-state baseline (lq_fp32_decode_step) on the same head-states and
+    tokens: mean time of one decode token over `tokens` launches."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    N = wl.n_states
+    cfg = lq.config(kda=wl.kda)
+    S0, _ = wlm.initial_state(wl)
+    S = torch.from_numpy(S0).to(device) if S0 is not None else torch.zeros((N, wl.dv, wl.dk), device=device)
+    del S0
+    pool = Pool(wl, 16, device)
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+
+    def launch(t):
+        q, k, v, a, b = pool.token(t)
+        lq.fp32_decode_step(cfg, S, N, q, k, v, a, b, o)
+
+    for t in range(warmup):
+        launch(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(tokens):
+        launch(t)
+    e1.record()
+    torch.cuda.synchronize()
+    if not torch.isfinite(o).all():
+        raise RuntimeError("non-finite fp32 baseline output")
+    ms = e0.elapsed_time(e1) / tokens
+    del S, pool, o
+    torch.cuda.empty_cache()
+    return ms
+
+
 def time_e2e(wl, steps, device):
     """End to end through the C ABI with host buffers: each step copies that
     window's inputs from pinned host memory, runs the 16 decode calls and copies
@@ -485,6 +528,18 @@ def run_ours(args):
             "fold_step_us": round(fold_ms * 1e3, 2), "window_gbs": round(win_gbs, 1),
             "window_frac": round(win_gbs / hbm, 4)}
         result["batches"] = sweep
+    if rank == 0 and not args.no_fp32:
+        f_ms = time_fp32(wl, device)
+        fb = N * alg_bytes_fp32(wl.kda)
+        int8_token_ms = t_ms / K / W
+        result["fp32_baseline"] = {
+            "kernel": "k_fp32_step (whole fp32 state, plain delta rule, one token per launch)",
+            "launch_ms": round(f_ms, 5), "head_tokens_per_s": round(N / (f_ms / 1e3), 1),
+            "alg_bytes_per_launch": fb, "achieved_gbs": round(fb / (f_ms / 1e3) / 1e9, 1),
+            "frac": round(fb / (f_ms / 1e3) / 1e9 / hbm, 4),
+            "int8_speedup_per_token": round(f_ms / int8_token_ms, 3),
+            "note": "same head-states, initial states and tokens as the int8 path; speedup = fp32 ms per token / "
+                    "int8 window ms / 16"}
     if rank == 0 and args.e2e_steps > 0:
         ms, h2d, d2h = time_e2e(wl, args.e2e_steps, device)
         result["e2e"] = {"value": round(N * W * args.e2e_steps / (ms / 1e3), 1), "unit": UNIT,
@@ -562,6 +617,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp32", action="store_true", help="skip the fp32-state baseline kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -153,6 +153,21 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
 int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, float* S_out, lq_stream_t stream);
 
 /*
+ * The fp32-state baseline: one decode token of the plain delta rule on whole
+ * fp32 states, the "FP32 kernel" that LeapQuant's kernel speedups are measured
+ * against ([LQ] §4.3; the update is §3.1 and App. A):
+ *   u = beta (v - S (alpha . k)),  S <- S Diag(alpha) + u k^T,  o = S q.
+ * S: fp32 [n_states][d_v][d_k] on the device, read and written in place (it is
+ * not an lq state buffer: no header, codes or records). Token arguments as
+ * lq_append; only cfg->d_k, d_v and decay_per_key are used. The summation
+ * order is not pinned: results are compared with a tolerance. Errors:
+ * LQ_ERR_INVALID_ARG for bad pointers, sizes or overlaps; nothing is checked on
+ * the device.
+ */
+int lq_fp32_decode_step(const lq_config* cfg, float* S, int64_t n_states, const float* q, const float* k,
+                        const float* v, const float* alpha, const float* beta, float* o, lq_stream_t stream);
+
+/*
  * Synchronize `stream`, then read the state buffer's status word: LQ_OK or the
  * first device-side error recorded since lq_state_init / lq_clear_status.
  * *bad_state (if non-NULL) receives the index of the head-state that set it.

@@ -568,3 +568,52 @@ int orc_run(const orc_cfg* cfg, orc_batch* b, int64_t n_tok, const float* q, con
   }
   return rc;
 }
+
+/*
+ * fp32-state baseline: the plain per-token delta rule with the state kept
+ * whole ([LQ] §3.1 and App. A: S_t = S_{t-1} Diag(alpha_t) + u_t k_t^T with
+ * u_t = beta_t (v_t - S_{t-1}(alpha_t . k_t)), o_t = S_t q_t; the "fp32
+ * kernel" the paper's kernel speedups are measured against, [LQ] §4.3).
+ * Evaluated in double for every head-state and token, T tokens in order.
+ * S: [n][d_v][d_k] double, updated in place; inputs token-major as in
+ * orc_run (q, k [T][n][d_k], v [T][n][d_v], alpha [T][n] or [T][n][d_k],
+ * beta [T][n]); o: [T][n][d_v] double (may be NULL).
+ */
+void orc_fp32_run(int32_t dk, int32_t dv, int32_t decay_per_key, int64_t n, int64_t T, double* S, const float* q,
+                  const float* k, const float* v, const float* alpha, const float* beta, double* o) {
+  const int alen = decay_per_key ? dk : 1;
+  double* r = (double*)malloc(sizeof(double) * (size_t)dv);
+  double* u = (double*)malloc(sizeof(double) * (size_t)dv);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t s = 0; s < n; ++s) {
+      double* Ss = S + (size_t)s * dv * dk;
+      const float* qs = q + ((size_t)t * n + s) * dk;
+      const float* ks = k + ((size_t)t * n + s) * dk;
+      const float* vs = v + ((size_t)t * n + s) * dv;
+      const float* as = alpha + ((size_t)t * n + s) * alen;
+      const double bs = beta[(size_t)t * n + s];
+      /* read: r = S_{t-1} (alpha . k) */
+      for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += Ss[(size_t)i * dk + j] * ((double)as[alen == 1 ? 0 : j] * (double)ks[j]);
+        r[i] = acc;
+      }
+      /* delta-rule correction and write */
+      for (int i = 0; i < dv; ++i) u[i] = bs * ((double)vs[i] - r[i]);
+      for (int i = 0; i < dv; ++i)
+        for (int j = 0; j < dk; ++j)
+          Ss[(size_t)i * dk + j] = Ss[(size_t)i * dk + j] * (double)as[alen == 1 ? 0 : j] + u[i] * (double)ks[j];
+      /* output o_t = S_t q_t */
+      if (o) {
+        double* os = o + ((size_t)t * n + s) * dv;
+        for (int i = 0; i < dv; ++i) {
+          double acc = 0.0;
+          for (int j = 0; j < dk; ++j) acc += Ss[(size_t)i * dk + j] * (double)qs[j];
+          os[i] = acc;
+        }
+      }
+    }
+  }
+  free(r);
+  free(u);
+}

@@ -77,6 +77,9 @@ def lib():
         L.orc_export.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P]
         L.orc_run.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P, _P, _P, _P, _P, _P,
                               ctypes.c_int, ctypes.c_int]
+        L.orc_fp32_run.restype = None
+        L.orc_fp32_run.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P,
+                                   _P, _P, _P, _P, _P, _P]
         _lib = L
     return _lib
 
@@ -209,3 +212,16 @@ class OracleState:
             else:
                 B[:, cid - self.dv] += self.comp_line[s, c, :self.dv]
         return B
+
+
+def fp32_run(S0, q, k, v, alpha, beta, want_o=True):
+    """The fp32-state baseline recurrence (plain per-token delta rule, whole state),
+    evaluated in double. S0 [n][d_v][d_k]; inputs token-major. Returns (S_T, o [T][n][d_v])."""
+    q, k, v, alpha, beta = (_f32(x) for x in (q, k, v, alpha, beta))
+    T, n, dk = q.shape
+    dv = v.shape[2]
+    S = np.ascontiguousarray(S0, dtype=np.float64).copy()
+    o = np.empty((T, n, dv), np.float64) if want_o else None
+    lib().orc_fp32_run(dk, dv, int(alpha.ndim == 3), n, T, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                       _ptr(o) if want_o else None)
+    return S, o

@@ -316,6 +316,32 @@ int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, f
   return launched(lqi::launch_export(p, (cudaStream_t)stream), "lq_export_state launch");
 }
 
+int lq_fp32_decode_step(const lq_config* cfg, float* S, int64_t n_states, const float* q, const float* k,
+                        const float* v, const float* alpha, const float* beta, float* o, lq_stream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_n(n_states))) return rc;
+  if (n_states == 0) return ok();
+  int dev = 0;
+  if ((rc = current_device(&dev)) || (rc = check_stream(stream, dev))) return rc;
+  if ((rc = check_ptr(S, "S", 16, dev))) return rc;
+  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o))) return rc;
+  const size_t sb = (size_t)n_states * kD * kD * sizeof(float), vec = (size_t)n_states * kD * sizeof(float);
+  if (overlaps(S, sb, o, vec) || overlaps(S, sb, q, vec) || overlaps(S, sb, k, vec) || overlaps(S, sb, v, vec))
+    return fail(LQ_ERR_INVALID_ARG, "S overlaps a token input or o");
+  lqi::Fp32Params p;
+  p.n_states = n_states;
+  p.kda = cfg->decay_per_key;
+  p.S = S;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.o = o;
+  return launched(lqi::launch_fp32_step(p, (cudaStream_t)stream), "lq_fp32_decode_step launch");
+}
+
 int lq_get_status(const void* state, int64_t* bad_state, lq_stream_t stream) {
   int dev = 0;
   int rc = current_device(&dev);

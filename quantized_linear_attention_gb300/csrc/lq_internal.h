@@ -34,7 +34,7 @@ struct Stage {
   // staged by bulk copies, dense
   int codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha;
   // computed, blocked layout
-  int kn_b, qn_b, y_b, aq_b, zk_b, zq_b, lam_b, kd_b, bd_b, P_b;
+  int kn_b, qn_b, zk_b, zq_b, lam_b, kd_b, bd_b, P_b;
   // computed, dense
   int basek, baseq, P, g, h, ec, eq, ca;
   int end;
@@ -70,10 +70,24 @@ struct Params {
   int r1;           // bytes of the staging / state-tile region
 };
 
+// The fp32-state baseline decode step (lq_fp32_decode_step).
+struct Fp32Params {
+  int64_t n_states;
+  int kda;
+  float* S;  // [n][d_v][d_k], updated in place
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* alpha;
+  const float* beta;
+  float* o;
+};
+
 cudaError_t launch_init(const Params& p, cudaStream_t st);
 cudaError_t launch_append(const Params& p, cudaStream_t st);
 cudaError_t launch_step(const Params& p, cudaStream_t st);
 cudaError_t launch_fold(const Params& p, cudaStream_t st);
 cudaError_t launch_export(const Params& p, cudaStream_t st);
+cudaError_t launch_fp32_step(const Fp32Params& p, cudaStream_t st);
 
 }  // namespace lqi

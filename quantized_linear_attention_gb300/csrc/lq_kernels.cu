@@ -60,7 +60,9 @@ __device__ __forceinline__ float code_f(uint32_t biased_word, int b) {
 
 // Packed fp32 pairs (the .f32x2 forms of mul / fma): each half is the
 // round-to-nearest IEEE result of its own lane, subnormals kept, so one pair
-// instruction is exactly two scalar operations issued at once.
+// instruction is exactly two scalar operations issued at once. They are used
+// only where no multiply feeds an add: the PTX assembler may fuse a packed
+// multiply and a following packed add into one fma, which rounds once.
 typedef unsigned long long f32x2;  // low half = first element
 
 __device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
@@ -79,11 +81,6 @@ __device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
 __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   f32x2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
@@ -279,8 +276,6 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.rec_alpha = take(kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
   L.kn_b = take(va * 4 * kBV);
   L.qn_b = take(va * 4 * kBV);
-  L.y_b = take(va * 4 * kBV);
-  L.aq_b = take(va * 4 * kBV);
   L.zk_b = take(va * 4 * kBV);
   L.zq_b = take(va * 4 * kBV);
   L.lam_b = take(fo * 4 * kBV);
@@ -454,8 +449,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   float* P_b = at<float>(sm, L.P_b);
   float* kn_b = at<float>(sm, L.kn_b);
   float* qn_b = at<float>(sm, L.qn_b);
-  float* y_b = at<float>(sm, L.y_b);
-  float* aq_b = at<float>(sm, L.aq_b);
   float* zk_b = at<float>(sm, L.zk_b);
   float* zq_b = at<float>(sm, L.zq_b);
   float* basek = at<float>(sm, L.basek);
@@ -521,8 +514,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     const float qa = __fmul_rn(A, tk.q);
     kn_b[jb] = tk.k;
     qn_b[jb] = tk.q;
-    y_b[jb] = yy;
-    aq_b[jb] = qa;
     zk_b[jb] = __fmul_rn(lam[j], yy);
     zq_b[jb] = __fmul_rn(lam[j], qa);
   }
@@ -531,6 +522,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
   // compensators, then k_n . q_n (the new record's output term, P_n = 1).
   // The k-side sums (g, ec) are pinned; the q-side (h, eq) only feeds o.
+  // Record m's sums sit at g[m-1], h[m-1]; k_n . q_n at h[n-1].
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
@@ -577,21 +569,32 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
             }
           }
         } else if (job < nrec + p.C) {
+          // y = A_n . k_n and A_n . q_n, formed again from the blocked k and q
           const int c = job - nrec;
           const int id = cid[c];
           const float4* b4 = reinterpret_cast<const float4*>(cl + c * kD + 16 * qq);
-          const float4* y4 = reinterpret_cast<const float4*>(y_b + 20 * qq);
-          const float4* a4 = reinterpret_cast<const float4*>(aq_b + 20 * qq);
+          const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
+          const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
+          const float4* a04 = reinterpret_cast<const float4*>(P_b + 20 * qq);
+          const float a0s = KDA ? 0.0f : P[0];
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 bb = b4[c4], yv = y4[c4], av = a4[c4];
+            const float4 bb = b4[c4], kx = kx4[c4], qx = qx4[c4];
             float bs[4] = {bb.x, bb.y, bb.z, bb.w};
-            const float ys[4] = {yv.x, yv.y, yv.z, yv.w}, as[4] = {av.x, av.y, av.z, av.w};
+            const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            float av[4] = {a0s, a0s, a0s, a0s};
+            if (KDA) {
+              const float4 a0 = a04[c4];
+              av[0] = a0.x;
+              av[1] = a0.y;
+              av[2] = a0.z;
+              av[3] = a0.w;
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
-              pa = __fmaf_rn(bs[e], ys[e], pa);
-              pb = __fmaf_rn(bs[e], as[e], pb);
+              pa = __fmaf_rn(bs[e], __fmul_rn(av[e], kxs[e]), pa);
+              pb = __fmaf_rn(bs[e], __fmul_rn(av[e], qxs[e]), pb);
             }
           }
         } else {
@@ -611,13 +614,13 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       pb = tree8(pb);
       if (job < njobs && qq == 0) {
         if (job < nrec) {
-          g[job + 1] = pa;
-          h[job + 1] = KDA ? pb : __fmul_rn(P[job + 1], pb);
+          g[job] = pa;
+          h[job] = KDA ? pb : __fmul_rn(P[job + 1], pb);
         } else if (job < nrec + p.C) {
           ec[job - nrec] = pa;
           eq[job - nrec] = pb;
         } else {
-          h[n] = pb;
+          h[n - 1] = pb;
         }
       }
     }
@@ -678,10 +681,10 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   }
   __syncthreads();
 
-  // A3-A5 per value row: acc = base; compensators in order; records in order;
+  // A3-A5 per value row: acc = base; compensators in order, each as its
+  // expanded rank-one term (a_c[i] is the column compensator's line entry, or
+  // 1 / 0 on / off a row compensator's row); records in order;
   // u_n = beta (v - acc). A6: the output in any order. A7: store record n.
-  // A row compensator's coefficient a_c[i] is zero except on its own row, and
-  // fma(0, x, acc) returns acc for the finite, never negative-zero acc here.
   if (tid < kD) {
     const int i = tid;
     float* ru = at<float>(sm, L.rec_u);
@@ -692,25 +695,28 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     for (int c = 0; c < kMaxC; ++c) {
       if (c < p.C) {
         const int id = cid[c];
-        if (id >= kD) {
-          const float a = cl[c * kD + i];
-          acc = __fmaf_rn(a, ec[c], acc);
-          oo = __fmaf_rn(a, eq[c], oo);
-        } else if (id == i) {
-          acc = __fmaf_rn(1.0f, ec[c], acc);
-          oo = __fmaf_rn(1.0f, eq[c], oo);
+        const float a = id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f);
+        acc = __fmaf_rn(a, ec[c], acc);
+        oo = __fmaf_rn(a, eq[c], oo);
+      }
+    }
+    // Records m = 1..n-1 in order, their dot products read four at a time.
+    const float* rui = ru + i;
+    for (int m0 = 0; m0 < n - 1; m0 += 4) {
+      const float4 g4 = *reinterpret_cast<const float4*>(g + m0);
+      const float4 h4 = *reinterpret_cast<const float4*>(h + m0);
+      const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, hs[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (m0 + e < n - 1) {
+          const float um = rui[(m0 + e) * kD];
+          acc = __fmaf_rn(um, gs[e], acc);
+          oo = __fmaf_rn(um, hs[e], oo);
         }
       }
     }
-    const float* rui = ru + i;
-#pragma unroll 4
-    for (int m = 1; m <= n - 1; ++m) {
-      const float um = rui[(m - 1) * kD];
-      acc = __fmaf_rn(um, g[m], acc);
-      oo = __fmaf_rn(um, h[m], oo);
-    }
     const float u = __fmul_rn(beta, __fsub_rn(tk.v, acc));
-    oo = __fmaf_rn(u, h[n], oo);
+    oo = __fmaf_rn(u, h[n - 1], oo);
     p.rec_u[rec_off + i] = u;
     p.o[s * kD + i] = oo;
     p.rec_k[rec_off + i] = tk.k;
@@ -783,23 +789,24 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   const float* U = at<float>(sm, L.rec_u);
   f32x2 a2[4][8];
   {
-    // lambda and P_0 pairs are read per row (8-byte loads) to keep registers
-    // for the 32 accumulator pairs.
-    const f32x2* lam2 = reinterpret_cast<const f32x2*>(at<float>(sm, L.lam_b) + 20 * qq);
-    const f32x2* p02 = reinterpret_cast<const f32x2*>(P_b + 20 * qq);
-    const f32x2 p0s = f2_pack(P[0], P[0]);
+    // The base in scalar multiplies (never contracted with what follows), then
+    // packed into pairs; lambda and P_0 are read per row to keep registers for
+    // the 32 accumulator pairs.
+    const float* lam = at<float>(sm, L.lam_b) + 20 * qq;
+    const float* p0b = P_b + 20 * qq;
     const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
-      const f32x2 s2 = f2_pack(sg[i], sg[i]);
-      const int4 c = *reinterpret_cast<const int4*>(cb + i * kD);
-      const uint32_t cw[4] = {(uint32_t)c.x ^ 0x80808080u, (uint32_t)c.y ^ 0x80808080u, (uint32_t)c.z ^ 0x80808080u,
-                              (uint32_t)c.w ^ 0x80808080u};
+      const float s_i = sg[i];
+      float f[16];
+      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const f32x2 f = code_pair(cw[k >> 1], (2 * k) & 3, cw[k >> 1], (2 * k + 1) & 3);
-        a2[pp][k] = f2_mul(f2_mul(f2_mul(s2, f), lam2[k]), KDA ? p02[k] : p0s);
+        const float2 l2 = *reinterpret_cast<const float2*>(lam + 2 * k);
+        const float2 q2 = KDA ? *reinterpret_cast<const float2*>(p0b + 2 * k) : make_float2(P[0], P[0]);
+        a2[pp][k] = f2_pack(__fmul_rn(__fmul_rn(__fmul_rn(s_i, f[2 * k]), l2.x), q2.x),
+                            __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[2 * k + 1]), l2.y), q2.y));
       }
     }
   }

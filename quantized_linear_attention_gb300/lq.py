@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
 
 # Every symbol include/lq.h declares.
 EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_append", "lq_fold",
-           "lq_decode_step", "lq_export_state", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
+           "lq_decode_step", "lq_export_state", "lq_fp32_decode_step", "lq_get_status", "lq_clear_status",
+           "lq_last_error", "lq_version")
 
 
 class Config(ctypes.Structure):
@@ -79,6 +80,7 @@ def load():
         "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
         "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
         "lq_export_state": (ctypes.c_int, [cfgp, P, i64, P, P]),
+        "lq_fp32_decode_step": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_get_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), P]),
         "lq_clear_status": (ctypes.c_int, [P, P]),
         "lq_last_error": (ctypes.c_char_p, []),
@@ -187,6 +189,14 @@ def decode_step(cfg, state, n_states, q, k, v, alpha, beta, o, phase=PHASE_ANY, 
 def export_state(cfg, state, n_states, S_out, stream=None):
     _check(load().lq_export_state(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(S_out, "S_out", _f32()),
                                   _stream(stream)))
+
+
+def fp32_decode_step(cfg, S, n_states, q, k, v, alpha, beta, o, stream=None):
+    """The fp32-state baseline: one plain delta-rule token on whole fp32 states S [n][d_v][d_k], in place."""
+    f = _f32()
+    _check(load().lq_fp32_decode_step(ctypes.byref(cfg), _ptr(S, "S", f), n_states, _ptr(q, "q", f), _ptr(k, "k", f),
+                                      _ptr(v, "v", f), _ptr(alpha, "alpha", f), _ptr(beta, "beta", f),
+                                      _ptr(o, "o", f), _stream(stream)))
 
 
 def get_status(state, stream=None):

@@ -22,7 +22,7 @@ def L():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "lq.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lq_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(lq_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(L):
