@@ -36,7 +36,7 @@ struct Stage {
   // computed, blocked layout
   int kn_b, qn_b, zk_b, zq_b, lam_b, kd_b, bd_b, P_b;
   // computed, dense
-  int basek, baseq, P, g, h, ec, eq, ca;
+  int basek, baseq, P, g, h, ec, eq;
   int end;
 };
 

@@ -83,6 +83,11 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
   f32x2 d;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -289,7 +294,6 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.h = take(4 * (W + 1));
   L.ec = take(4 * (C > 0 ? C : 1));
   L.eq = take(4 * (C > 0 ? C : 1));
-  L.ca = take(fo * 4 * kD * C);
   L.end = o;
   return L;
 }
@@ -742,9 +746,8 @@ namespace lqi {
 // sqrt(mean |.|) with a floor; then one rounding to int8 per row step.
 // 256 threads; a thread owns rows 32pp + 4w + r (pp = 0..3), columns 16qq..16qq+15.
 
-// F0: record keys scaled by their decay products (kd_m = P_m . k_m), the
-// expanded compensators (a_c, P_0 . b_c) and lambda, blocked where lanes read
-// them block-wise.
+// F0: record keys scaled by their decay products (kd_m = P_m . k_m), the row
+// compensators' P_0 . line, and lambda, blocked where lanes read them block-wise.
 template <bool KDA>
 __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage& L, char* sm) {
   const int tid = threadIdx.x;
@@ -752,25 +755,43 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
   const float* P_b = at<float>(sm, L.P_b);
   const float* rk = at<float>(sm, L.rec_k);
   float* kd_b = at<float>(sm, L.kd_b);
-#pragma unroll 4
-  for (int e = tid; e < n * kD; e += 256) {
-    const int m1 = e >> 7, j = e & (kD - 1);
-    kd_b[m1 * kBV + bv(j)] = __fmul_rn(decay_at<KDA>(P, P_b, m1 + 1, j), rk[e]);
+  // kd_m = P_m . k_m, four entries per step (blocks of 16 stay contiguous in
+  // the blocked layout, so each step is one 16-byte load and store).
+  for (int e4 = tid; e4 < n * (kD / 4); e4 += 256) {
+    const int m1 = e4 >> 5, j4 = (e4 & 31) << 2;
+    const float4 kv = *reinterpret_cast<const float4*>(rk + m1 * kD + j4);
+    float4 pm;
+    if (KDA) {
+      pm = *reinterpret_cast<const float4*>(P_b + (m1 + 1) * kBV + bv(j4));
+    } else {
+      const float x = P[m1 + 1];
+      pm = make_float4(x, x, x, x);
+    }
+    *reinterpret_cast<float4*>(kd_b + m1 * kBV + bv(j4)) =
+        make_float4(__fmul_rn(pm.x, kv.x), __fmul_rn(pm.y, kv.y), __fmul_rn(pm.z, kv.z), __fmul_rn(pm.w, kv.w));
   }
+  // bd_c = P_0 . line for the row compensators (a column compensator's b_c is
+  // a unit vector; its term is applied from the line and P_0 directly).
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
-  float* ca = at<float>(sm, L.ca);
   float* bd_b = at<float>(sm, L.bd_b);
-  for (int e = tid; e < p.C * kD; e += 256) {
-    const int c = e >> 7, x = e & (kD - 1);
-    const int id = cid[c];
-    const float lv = cl[e];
-    const float a = (id < kD) ? (x == id ? 1.0f : 0.0f) : lv;
-    const float b = (id < kD) ? lv : (x == id - kD ? 1.0f : 0.0f);
-    ca[e] = a;
-    bd_b[c * kBV + bv(x)] = __fmul_rn(decay_at<KDA>(P, P_b, 0, x), b);
+  if (tid < p.C * (kD / 4)) {
+    const int c = tid >> 5, j4 = (tid & 31) << 2;
+    if (cid[c] < kD) {
+      const float4 lv = *reinterpret_cast<const float4*>(cl + c * kD + j4);
+      float4 p0;
+      if (KDA) {
+        p0 = *reinterpret_cast<const float4*>(P_b + bv(j4));
+      } else {
+        p0 = make_float4(P[0], P[0], P[0], P[0]);
+      }
+      *reinterpret_cast<float4*>(bd_b + c * kBV + bv(j4)) =
+          make_float4(__fmul_rn(p0.x, lv.x), __fmul_rn(p0.y, lv.y), __fmul_rn(p0.z, lv.z), __fmul_rn(p0.w, lv.w));
+    }
   }
-  if (tid < kD) at<float>(sm, L.lam_b)[bv(tid)] = at<float>(sm, L.lambda)[tid];
+  if (tid < kD / 4)
+    *reinterpret_cast<float4*>(at<float>(sm, L.lam_b) + bv(4 * tid)) =
+        *reinterpret_cast<const float4*>(at<float>(sm, L.lambda) + 4 * tid);
   __syncthreads();
 }
 
@@ -983,11 +1004,12 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   if (tid < kD) tl.score[kD + tid] = tree8_mem(tl.colpart + tid, kD);
   __syncthreads();
 
-  // F2: C greedy rounds of the longest line, ties to the smallest id. Every
-  // warp finds the winner itself from this round's scores (lane L scans ids L,
-  // L+32, ... in ascending order, then a butterfly keeps the larger score, the
-  // smaller id on a tie). The next round's scores go to the other score array,
-  // so nothing a round reads is written during it. Then, in parallel:
+  // F2: C greedy rounds of the longest line, ties to the smallest id. Warp 0
+  // finds the winner from this round's scores (lane L scans ids L, L+32, ...
+  // in ascending order, then a butterfly keeps the larger score, the smaller
+  // id on a tie) and publishes it. The next round's scores go to the other
+  // score array, so nothing a round reads is written during it. Then, in
+  // parallel:
   //  - threads 0..127 refresh the scores the taken line changes: taking row i*
   //    changes the block i*/16 partial of every column; taking column j*
   //    changes the block j*/16 partial of every row. The refresh skips the
@@ -996,31 +1018,36 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   //  - threads 128..255 carry the unchanged scores over (the taken line's
   //    becomes 0), copy the line out exactly, zero it in the tile and clear its
   //    partials.
-  // One barrier ends each round.
+  // Two barriers per round: after the winner is published, and at the end.
+  __shared__ int s_win;
   for (int c = 0; c < p.C; ++c) {
     const float* cur = (c & 1) ? tl.score2 : tl.score;
     float* nxt = (c & 1) ? tl.score : tl.score2;
-    const int L = tid & 31;
-    float bsc = cur[L];
-    int bi = L;
+    if (w == 0) {
+      const int L = tid & 31;
+      float bsc = cur[L];
+      int bi = L;
 #pragma unroll
-    for (int e = 1; e < 8; ++e) {
-      const float v = cur[L + 32 * e];
-      if (v > bsc) {
-        bsc = v;
-        bi = L + 32 * e;
+      for (int e = 1; e < 8; ++e) {
+        const float v = cur[L + 32 * e];
+        if (v > bsc) {
+          bsc = v;
+          bi = L + 32 * e;
+        }
       }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bsc || (ov == bsc && oi < bi)) {
-        bsc = ov;
-        bi = oi;
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bsc || (ov == bsc && oi < bi)) {
+          bsc = ov;
+          bi = oi;
+        }
       }
+      if (L == 0) s_win = bi;
     }
-    const int win = bi;
+    __syncthreads();
+    const int win = s_win;
     float* line = p.comp_line + (s * p.C + c) * kD;
     if (win < kD) {
       const int b = win >> 4;
@@ -1104,11 +1131,13 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
       mx[pp] = 0.0f;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
-        t[pp][4 * c4 + 0] = __fmul_rn(x.x, g[4 * c4 + 0]);
-        t[pp][4 * c4 + 1] = __fmul_rn(x.y, g[4 * c4 + 1]);
-        t[pp][4 * c4 + 2] = __fmul_rn(x.z, g[4 * c4 + 2]);
-        t[pp][4 * c4 + 3] = __fmul_rn(x.w, g[4 * c4 + 3]);
+        // t = R g in packed pairs: the product feeds a maximum and a scalar
+        // multiply, never an add, so it cannot be fused.
+        const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(&S[i * kD + roff[c4]]);
+        const f32x2 t0 = f2_mul(x.x, f2_pack(g[4 * c4 + 0], g[4 * c4 + 1]));
+        const f32x2 t1 = f2_mul(x.y, f2_pack(g[4 * c4 + 2], g[4 * c4 + 3]));
+        f2_unpack(t0, t[pp][4 * c4 + 0], t[pp][4 * c4 + 1]);
+        f2_unpack(t1, t[pp][4 * c4 + 2], t[pp][4 * c4 + 3]);
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) mx[pp] = fmaxf(mx[pp], fabsf(t[pp][e]));
