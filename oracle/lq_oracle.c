@@ -53,8 +53,10 @@ typedef struct {
   int32_t C;             /* number of compensators                                */
   int32_t decay_per_key; /* 0: scalar alpha (GDN); 1: alpha in R^{d_k} (KDA)      */
   int32_t smooth;        /* 1: residual smoothing on                              */
-  int32_t quantize;      /* 1: int8 boundary; 0: fp32 boundary, C must be 0      */
+  int32_t quantize;      /* 1: low-bit boundary; 0: fp32 boundary, C must be 0   */
   float lambda_floor;    /* positive floor of the smoothing scales               */
+  int32_t code_bits;     /* code width b (2..8): codes in [-qmax, qmax],         */
+                         /* qmax = 2^(b-1) - 1 ([LQ] §4: 8-, 6- and 4-bit states) */
 } orc_cfg;
 
 /* Batch storage; every array holds n_states consecutive per-state blocks. */
@@ -362,9 +364,11 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
     st.lambda[j] = lam;
     g[j] = 1.0f / lam;
   }
-  /* F4-F5: t = R Diag(g); per-row absmax m_i; sigma_i = m_i / 127 and the
-   * reciprocal h_i = 127 / m_i once per row; codes = clamp(rint(t * h), -127, 127).
-   * An all-zero row gets sigma = 0 and zero codes. */
+  /* F4-F5: t = R Diag(g); per-row absmax m_i; sigma_i = m_i / qmax and the
+   * reciprocal h_i = qmax / m_i once per row; codes = clamp(rint(t * h), -qmax,
+   * qmax) (qmax = 127 for 8-bit codes). An all-zero row gets sigma = 0 and zero
+   * codes. */
+  const float qmax = (float)((1 << (cfg->code_bits - 1)) - 1);
   for (int i = 0; i < dv; ++i) {
     float mx = 0.0f;
     for (int j = 0; j < dk; ++j) {
@@ -373,8 +377,8 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
     }
     float sig = 0.0f, h = 0.0f;
     if (mx != 0.0f) {
-      sig = mx / 127.0f;
-      h = 127.0f / mx;
+      sig = mx / qmax;
+      h = qmax / mx;
     }
     st.sigma[i] = sig;
     for (int j = 0; j < dk; ++j) {
@@ -382,8 +386,8 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
       float s = t * h;
       if (dg && dg->s_round) dg->s_round[(size_t)i * dk + j] = s;
       float r = nearbyintf(s);
-      if (r > 127.0f) r = 127.0f;
-      if (r < -127.0f) r = -127.0f;
+      if (r > qmax) r = qmax;
+      if (r < -qmax) r = -qmax;
       st.codes[(size_t)i * dk + j] = (int8_t)r;
     }
   }
@@ -459,6 +463,7 @@ static int cfg_ok(const orc_cfg* c) {
   if (c->W < 1 || c->W > 4096 || c->C < 0 || c->C > 64) return 0;
   if (!c->quantize && c->C != 0) return 0;
   if (!(c->lambda_floor > 0.0f)) return 0;
+  if (c->code_bits < 2 || c->code_bits > 8) return 0;
   return 1;
 }
 

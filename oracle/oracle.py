@@ -29,6 +29,7 @@ class Cfg(ctypes.Structure):
         ("smooth", ctypes.c_int32),
         ("quantize", ctypes.c_int32),
         ("lambda_floor", ctypes.c_float),
+        ("code_bits", ctypes.c_int32),
     ]
 
 
@@ -118,11 +119,12 @@ class OracleState:
     """Boundary + record buffer for ``n_states`` head-states, as numpy arrays."""
 
     def __init__(self, n_states, dk=128, dv=128, W=16, C=4, decay_per_key=False, smooth=True, quantize=True,
-                 lambda_floor=1e-6):
+                 lambda_floor=1e-6, code_bits=8):
         self.n, self.dk, self.dv, self.W, self.C = int(n_states), int(dk), int(dv), int(W), int(C)
         self.kda = bool(decay_per_key)
+        self.code_bits = int(code_bits)
         self.cfg = Cfg(self.dk, self.dv, self.W, self.C, int(decay_per_key), int(smooth), int(quantize),
-                       float(lambda_floor))
+                       float(lambda_floor), self.code_bits)
         N, L = self.n, max(self.dk, self.dv)
         alen = self.dk if self.kda else 1
         self.codes = np.zeros((N, self.dv, self.dk), np.int8)

@@ -102,14 +102,17 @@ def test_pin1_windowed_unquantized_equals_plain_recurrence(case):
 
 
 # ---------------------------------------------------------------- PIN-2
-def test_pin2_window1_no_comp_no_smooth_is_naive_per_token_rounding():
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_pin2_window1_no_comp_no_smooth_is_naive_per_token_rounding(bits):
     """W = 1, C = 0, smoothing off is the naive scheme: round after every token
-    (research note 4, "Why rounding the state is difficult"). The naive side is
-    written here in numpy float32, independently; compared in lockstep."""
+    (research note 4, "Why rounding the state is difficult"), at 8-, 6- and
+    4-bit codes (LeapQuant §4). The naive side is written here in numpy float32,
+    independently; compared in lockstep."""
+    qm = 2 ** (bits - 1) - 1
     wl = wlm.custom(101, 4, 48, n_warm=64)
     S0, _ = wlm.initial_state(wl)
     tk = wlm.tokens(wl, 0, wl.n_tokens)
-    st = OracleState(wl.n_states, W=1, C=0, smooth=False)
+    st = OracleState(wl.n_states, W=1, C=0, smooth=False, code_bits=bits)
     st.init(S0)
     f32 = np.float32
     total = 0
@@ -122,9 +125,9 @@ def test_pin2_window1_no_comp_no_smooth_is_naive_per_token_rounding():
         u = (beta[:, None] * (v - r)).astype(f32)
         Snew = (a[:, None, None] * Sprev + u[:, :, None] * k[:, None, :]).astype(f32)
         m = np.abs(Snew).max(axis=2)
-        h = np.where(m > 0, f32(127) / np.where(m > 0, m, 1), 0).astype(f32)
+        h = np.where(m > 0, f32(qm) / np.where(m > 0, m, 1), 0).astype(f32)
         s = (Snew * h[:, :, None]).astype(f32)
-        codes_naive = np.clip(np.rint(s), -127, 127).astype(np.int8)
+        codes_naive = np.clip(np.rint(s), -qm, qm).astype(np.int8)
         o_naive = np.einsum("nij,nj->ni", Snew.astype(np.float64), q.astype(np.float64))
 
         o = st.run(q[None], k[None], v[None], a[None], beta[None])[0]
@@ -132,7 +135,8 @@ def test_pin2_window1_no_comp_no_smooth_is_naive_per_token_rounding():
         n, ok = code_mismatches(st.codes, codes_naive, s, rel=0.0, abs_=1e-4)
         assert ok, t
         total += n
-        np.testing.assert_allclose(st.sigma, m / f32(127), rtol=3e-7, atol=0)
+        np.testing.assert_allclose(st.sigma, m / f32(qm), rtol=3e-7, atol=0)
+        assert np.abs(st.codes).max() <= qm
     assert total <= 1e-3 * wl.n_tokens * st.codes.size
 
 
@@ -206,13 +210,14 @@ def test_pin3_d4_brute_force(kda):
 
 # ---------------------------------------------------------------- PIN-4
 @pytest.mark.parametrize("wid", [1, 5])
-def test_pin4_half_step_reconstruction_after_every_fold(wid):
+@pytest.mark.parametrize("bits", [8, 4])
+def test_pin4_half_step_reconstruction_after_every_fold(wid, bits):
     wl = wlm.WORKLOADS[wid]
     N = 2
     W = wl.W
     S0, _ = wlm.initial_state(wl, 0, N)
     tk = wlm.tokens(wl, 0, 3 * W, 0, N)
-    st = OracleState(N, W=W, C=4, decay_per_key=wl.kda)
+    st = OracleState(N, W=W, C=4, decay_per_key=wl.kda, code_bits=bits)
     dg0 = [FoldDiag(128, 128) for _ in range(N)]
     st.init(S0, diags=dg0)
     folds = [dg0]
@@ -356,18 +361,20 @@ def test_pin9_power_of_two_scale_invariance():
 
 
 # ---------------------------------------------------------------- textbook special cases
-def test_no_comp_no_smooth_init_is_textbook_per_row_absmax():
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_no_comp_no_smooth_init_is_textbook_per_row_absmax(bits):
+    qm = 2 ** (bits - 1) - 1
     rng = np.random.default_rng(11)
     S0 = (rng.standard_normal((4, 128, 128)) * rng.uniform(0.1, 10, (4, 128, 1))).astype(np.float32)
     S0[1, 5, :] = 0.0  # all-zero row: sigma 0, codes 0
-    st = OracleState(4, C=0, smooth=False)
+    st = OracleState(4, C=0, smooth=False, code_bits=bits)
     st.init(S0)
     f32 = np.float32
     m = np.abs(S0).max(axis=2)
-    h = np.where(m > 0, f32(127) / np.where(m > 0, m, 1), 0).astype(f32)
-    ref = np.clip(np.rint((S0 * h[:, :, None]).astype(f32)), -127, 127).astype(np.int8)
+    h = np.where(m > 0, f32(qm) / np.where(m > 0, m, 1), 0).astype(f32)
+    ref = np.clip(np.rint((S0 * h[:, :, None]).astype(f32)), -qm, qm).astype(np.int8)
     assert np.array_equal(st.codes, ref)
-    assert np.array_equal(st.sigma, np.where(m > 0, m / f32(127), 0).astype(f32))
+    assert np.array_equal(st.sigma, np.where(m > 0, m / f32(qm), 0).astype(f32))
     assert (st.codes[1, 5] == 0).all() and st.sigma[1, 5] == 0
 
 
