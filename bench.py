@@ -48,21 +48,21 @@ KERNEL_SOURCE = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc", "
 
 
 # ----------------------------------------------------------------------------- bytes
-def alg_bytes_append(p, C=4, kda=False, D=128):
+def alg_bytes_append(p, C=4, kda=False, D=128, bits=8):
     """Algorithmic bytes one head-state moves in an append at window phase p
     (p records held before the token): every input read once, every output written once."""
     alen = D if kda else 1
     rec = 4 * D + 4 * D + 4 * alen  # k, u, alpha of one record
-    reads = D * D + 4 * D + 4 * D + 4 * C + 4 * C * D  # boundary: codes, sigma, lambda, ids, lines
+    reads = D * D * bits // 8 + 4 * D + 4 * D + 4 * C + 4 * C * D  # boundary: codes, sigma, lambda, ids, lines
     reads += p * rec + 4  # buffered records, record count
     reads += 4 * D * 3 + 4 * alen + 4  # q, k, v, alpha, beta
     writes = rec + 4 * D + 4  # new record, o, record count
     return reads + writes
 
 
-def alg_bytes_fold_extra(C=4, D=128):
+def alg_bytes_fold_extra(C=4, D=128, bits=8):
     """Bytes the fold adds to the append that fills the window: the new boundary."""
-    return D * D + 4 * D + 4 * D + 4 * C + 4 * C * D
+    return D * D * bits // 8 + 4 * D + 4 * D + 4 * C + 4 * C * D
 
 
 def alg_bytes_fp32(kda=False, D=128):
@@ -71,9 +71,9 @@ def alg_bytes_fp32(kda=False, D=128):
     return 2 * 4 * D * D + 4 * D * 3 + 4 * (D if kda else 1) + 4 + 4 * D
 
 
-def alg_bytes_window(W=16, C=4, kda=False):
+def alg_bytes_window(W=16, C=4, kda=False, bits=8):
     """Per head-state per window: W-1 appends and one fused append+fold."""
-    return sum(alg_bytes_append(p, C, kda) for p in range(W)) + alg_bytes_fold_extra(C)
+    return sum(alg_bytes_append(p, C, kda, bits=bits) for p in range(W)) + alg_bytes_fold_extra(C, bits=bits)
 
 
 # ----------------------------------------------------------------------------- environment
@@ -237,13 +237,13 @@ class Pool:
         return [x[t] for x in self.dev]
 
 
-def setup_state(wl, device, state0=0):
+def setup_state(wl, device, state0=0, bits=8):
     import torch
 
     from quantized_linear_attention_gb300 import lq
     from quantized_linear_attention_gb300 import workload as wlm
 
-    cfg = lq.config(window=wl.W, n_comp=wl.C, kda=wl.kda)
+    cfg = lq.config(window=wl.W, n_comp=wl.C, kda=wl.kda, code_bits=bits)
     S0, _ = wlm.initial_state(wl, state0, wl.n_states)
     state = lq.alloc_state(cfg, wl.n_states, device)
     lq.state_init(cfg, state, wl.n_states, None if S0 is None else torch.from_numpy(S0).to(device))
@@ -251,7 +251,7 @@ def setup_state(wl, device, state0=0):
     return cfg, state
 
 
-def time_main(wl, args, device, world, rank=0):
+def time_main(wl, args, device, world, rank=0, bits=8, steps=None):
     """The timed region: K windows, a CUDA event between every two launches."""
     import torch
 
@@ -259,7 +259,7 @@ def time_main(wl, args, device, world, rank=0):
 
     W, N = wl.W, wl.n_states
     s0 = shard_offset(wl, rank)
-    cfg, state = setup_state(wl, device, s0)
+    cfg, state = setup_state(wl, device, s0, bits)
     pool = Pool(wl, 4 * W, device, state0=s0)
     o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
 
@@ -273,7 +273,7 @@ def time_main(wl, args, device, world, rank=0):
             launch(tok)
             tok += 1
     torch.cuda.synchronize()
-    K = args.steps
+    K = args.steps if steps is None else steps
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(K * W + 1)]
     sampler = ClockSampler(device.index or 0)
     time.sleep(0.3)
@@ -528,6 +528,18 @@ def run_ours(args):
             "fold_step_us": round(fold_ms * 1e3, 2), "window_gbs": round(win_gbs, 1),
             "window_frac": round(win_gbs / hbm, 4)}
         result["batches"] = sweep
+    if rank == 0 and not args.no_bits4:
+        b_total, b_app, b_fold, _ = time_main(wl, args, device, 1, 0, bits=4, steps=100)
+        b_app_ms, b_fold_ms, b_win_ms = statistics.mean(b_app), statistics.mean(b_fold), b_total / 100
+        bw = N * alg_bytes_window(W, wl.C, wl.kda, bits=4)
+        b_app_bytes = N * statistics.mean(alg_bytes_append(p, wl.C, wl.kda, bits=4) for p in range(W - 1))
+        result["code_bits_4"] = {
+            "note": "the same workload with 4-bit codes (two per byte); 100 timed windows",
+            "head_tokens_per_s": round(N * W / (b_win_ms / 1e3), 1), "append_step_us": round(b_app_ms * 1e3, 2),
+            "fold_step_us": round(b_fold_ms * 1e3, 2), "alg_bytes_per_head_token": round(bw / N / W, 1),
+            "window_gbs": round(bw / (b_win_ms / 1e3) / 1e9, 1), "window_frac": round(bw / (b_win_ms / 1e3) / 1e9 / hbm, 4),
+            "append_gbs": round(b_app_bytes / (b_app_ms / 1e3) / 1e9, 1),
+            "append_frac": round(b_app_bytes / (b_app_ms / 1e3) / 1e9 / hbm, 4)}
     if rank == 0 and not args.no_fp32:
         f_ms = time_fp32(wl, device)
         fb = N * alg_bytes_fp32(wl.kda)
@@ -618,6 +630,7 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp32", action="store_true", help="skip the fp32-state baseline kernel")
+    ap.add_argument("--no-bits4", action="store_true", help="skip the 4-bit-code run of the same workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

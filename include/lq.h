@@ -71,6 +71,8 @@ typedef struct {
   int32_t decay_per_key; /* 0: scalar alpha per token (GDN); 1: alpha in R^{d_k} (KDA)      */
   int32_t smooth;        /* 1: residual smoothing on (default); 0: lambda = 1               */
   float lambda_floor;    /* positive floor of the smoothing scales (default 1e-6)           */
+  int32_t code_bits;     /* code width: 8 (default) or 4 ([LQ] §4 also evaluates 6- and      */
+                         /* 4-bit states); codes in [-q, q], q = 2^(bits-1) - 1              */
 } lq_config;
 
 /*
@@ -78,7 +80,9 @@ typedef struct {
  * and the per-head-state stride of each plane, in elements. The buffer holds,
  * for head-state s:
  *   counts   int32   [s]                       records held (0..W)
- *   codes    int8    [s][d_v][d_k]             row-major
+ *   codes    int8    [s][d_v][d_k]             row-major (8-bit codes), or
+ *            uint8   [s][d_v][d_k / 2]         4-bit codes: two per byte, code 2j in the
+ *                                              low nibble, each stored as c + 8 (1..15)
  *   sigma    fp32    [s][d_v]                  quantization step of each value row
  *   lambda   fp32    [s][d_k]                  smoothing scale of each key channel
  *   comp_id  int32   [s][comp_id_stride]       id < d_v: row id; else column id - d_v
@@ -89,8 +93,9 @@ typedef struct {
  * A 256-byte header at offset 0 carries a magic number, a hash of the config
  * and n_states, and the device status word.
  * The boundary (codes, sigma, lambda, comp_id, comp_line) takes
- * (16384 + 512 + 512 + 4C + 512C) bytes per head-state: 1.19 bytes per element
- * at C = 4, the figure of the LeapQuant summary, §4.3 Efficiency results.
+ * (16384 + 512 + 512 + 4C + 512C) bytes per head-state with 8-bit codes: 1.19
+ * bytes per element at C = 4, the figure of the LeapQuant summary, §4.3
+ * Efficiency results (8192 + ... with 4-bit codes: 0.69 bytes per element).
  */
 typedef struct {
   size_t total_bytes;
@@ -100,7 +105,7 @@ typedef struct {
   int64_t boundary_bytes_per_state; /* codes + sigma + lambda + 4C id bytes + comp lines                  */
 } lq_layout_t;
 
-/* Default configuration: d_k = d_v = 128, W = 16, C = 4, GDN, smoothing on, floor 1e-6. */
+/* Default configuration: d_k = d_v = 128, W = 16, C = 4, GDN, smoothing on, floor 1e-6, 8-bit codes. */
 void lq_config_default(lq_config* cfg);
 
 /* Bytes the caller must allocate for n_states head-states (0 if cfg or n_states is invalid). */

@@ -43,6 +43,7 @@ struct Stage {
 // Everything a kernel needs, passed by value.
 struct Params {
   int W, C, kda, smooth;
+  int bits;  // code width: 8 or 4
   float lambda_floor;
   int phase;  // expected record count before the call, or -1
   int64_t n_states;

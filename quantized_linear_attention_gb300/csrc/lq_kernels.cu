@@ -50,13 +50,6 @@ __device__ __forceinline__ void set_error(const Params& p, int code, int64_t s) 
   if (atomicCAS(&p.hdr->status, 0, code) == 0) p.hdr->bad_state = s;
 }
 
-// Exact int8 -> fp32 for byte b of a word whose bytes were biased by ^0x80
-// (c + 128 in [0, 255]): place the byte in the mantissa of 2^23 and subtract
-// 2^23 + 128. Both steps are exact in IEEE fp32.
-__device__ __forceinline__ float code_f(uint32_t biased_word, int b) {
-  const uint32_t bits = __byte_perm(biased_word, 0x4B000000u, 0x7540u | (uint32_t)b);
-  return __fsub_rn(__uint_as_float(bits), 8388736.0f);
-}
 
 // Packed fp32 pairs (the .f32x2 forms of mul / fma): each half is the
 // round-to-nearest IEEE result of its own lane, subnormals kept, so one pair
@@ -102,11 +95,45 @@ __device__ __forceinline__ f32x2 code_pair(uint32_t w_lo, int b_lo, uint32_t w_h
                 bias);
 }
 
-__device__ __forceinline__ void codes16_to_float(int4 c, float f[16]) {
-  const uint32_t w[4] = {(uint32_t)c.x ^ 0x80808080u, (uint32_t)c.y ^ 0x80808080u, (uint32_t)c.z ^ 0x80808080u,
-                         (uint32_t)c.w ^ 0x80808080u};
-#pragma unroll
-  for (int t = 0; t < 16; ++t) f[t] = code_f(w[t >> 2], t & 3);
+// A lane's 16 codes of one row as four words of biased bytes, and the exact
+// conversion of code e (0..15) from them.
+//  8-bit codes (int8, 16 bytes): the words are the four code words with every
+//    byte biased by ^0x80 (c + 128).
+//  4-bit codes (8 bytes, nibble e of the block holds c + 8, low nibble first):
+//    the words are {lo0, hi0, lo1, hi1}, the even and odd nibbles of the two
+//    code words spread into bytes; element e sits in word 2(e/8) + (e & 1),
+//    byte (e & 7) / 2.
+// Each byte goes into the mantissa of 2^23 and the bias 2^23 + 128 (or 2^23 + 8)
+// is subtracted: both steps are exact.
+template <bool B4>
+__device__ __forceinline__ void code_words(const int8_t* row_block, uint32_t cw[4]) {
+  if (B4) {
+    const uint2 c = *reinterpret_cast<const uint2*>(row_block);
+    cw[0] = c.x & 0x0F0F0F0Fu;
+    cw[1] = (c.x >> 4) & 0x0F0F0F0Fu;
+    cw[2] = c.y & 0x0F0F0F0Fu;
+    cw[3] = (c.y >> 4) & 0x0F0F0F0Fu;
+  } else {
+    const int4 c = *reinterpret_cast<const int4*>(row_block);
+    cw[0] = (uint32_t)c.x ^ 0x80808080u;
+    cw[1] = (uint32_t)c.y ^ 0x80808080u;
+    cw[2] = (uint32_t)c.z ^ 0x80808080u;
+    cw[3] = (uint32_t)c.w ^ 0x80808080u;
+  }
+}
+
+template <bool B4>
+__device__ __forceinline__ float code_at(const uint32_t cw[4], int e) {
+  const uint32_t w = B4 ? cw[2 * (e >> 3) + (e & 1)] : cw[e >> 2];
+  const int b = B4 ? ((e & 7) >> 1) : (e & 3);
+  const uint32_t bits = __byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)b);
+  return __fsub_rn(__uint_as_float(bits), B4 ? 8388616.0f : 8388736.0f);
+}
+
+// Bytes of one row of codes, and of one lane's 16-code block.
+template <bool B4>
+__host__ __device__ constexpr int row_bytes() {
+  return B4 ? kD / 2 : kD;
 }
 
 // Sum of the 8 block partials of a lane group in the fixed tree order.
@@ -262,7 +289,7 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 // when the keys travel in registers). The token's q, k, v (and alpha) are read
 // into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
-                                              bool append, bool fold) {
+                                              bool append, bool fold, int bits) {
   Stage L;
   int o = 0;
   auto take = [&](int bytes) {
@@ -271,7 +298,7 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
     return at_;
   };
   const int va = append ? 1 : 0, fo = fold ? 1 : 0;
-  L.codes = take(kD * kD);
+  L.codes = take(kD * kD * bits / 8);
   L.sigma = take(4 * kD);
   L.lambda = take(4 * kD);
   L.comp_id = take(4 * comp_id_stride);
@@ -345,11 +372,12 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
                                             uint64_t* bar, bool stage_k) {
   const uint32_t rec = 4u * kD * (uint32_t)n0;
   const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
-  uint32_t bytes = kD * kD + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec;
+  const uint32_t code_bytes = (uint32_t)(kD * kD * p.bits / 8);
+  uint32_t bytes = code_bytes + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec;
   if (!p.kda || n0 > 0) bytes += alpha_bytes;
   if (stage_k) bytes += rec;
   mbar_expect_tx(bar, bytes);
-  bulk_g2s(sm + L.codes, p.codes + s * (kD * kD), kD * kD, bar);
+  bulk_g2s(sm + L.codes, p.codes + s * code_bytes, code_bytes, bar);
   bulk_g2s(sm + L.sigma, p.sigma + s * kD, 4 * kD, bar);
   bulk_g2s(sm + L.lambda, p.lambda + s * kD, 4 * kD, bar);
   bulk_g2s(sm + L.comp_id, p.comp_id + s * p.comp_id_stride, 4u * (uint32_t)p.comp_id_stride, bar);
@@ -440,7 +468,7 @@ __device__ __forceinline__ TokenRegs load_token(const Params& p, int64_t s) {
 // KPRE: record keys are not staged; lane group g arrives with block qq of
 // record slot g in `kpre` (read before the staging wait), and slots beyond the
 // first round of lane groups are read from global memory.
-template <bool KDA, int NT, bool FOLD, bool KPRE>
+template <bool KDA, int NT, bool FOLD, bool KPRE, bool B4>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                float alpha_scalar, float beta, const TokenRegs& tk,
                                                const float4 (&kpre)[4]) {
@@ -635,7 +663,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // time, 4 rows interleaved; each row's chain runs over its 16 elements in
   // ascending order, then the canonical tree (shared out over the lane group).
   {
-    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
+    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
     const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
     const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
     float v[2 * RPT];
@@ -643,13 +671,8 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     for (int half = 0; half < RPT / 4; ++half) {
       uint32_t cw[4][4];
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        const int4 c = *reinterpret_cast<const int4*>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * kD);
-        cw[pp][0] = (uint32_t)c.x ^ 0x80808080u;
-        cw[pp][1] = (uint32_t)c.y ^ 0x80808080u;
-        cw[pp][2] = (uint32_t)c.z ^ 0x80808080u;
-        cw[pp][3] = (uint32_t)c.w ^ 0x80808080u;
-      }
+      for (int pp = 0; pp < 4; ++pp)
+        code_words<B4>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<B4>(), cw[pp]);
       float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -659,7 +682,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         for (int pp = 0; pp < 4; ++pp) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float f = code_f(cw[pp][c4], e);
+            const float f = code_at<B4>(cw[pp], 4 * c4 + e);
             ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
             aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
           }
@@ -798,7 +821,7 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
 // F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
 // lambda_j) P_0[j], then the compensators in order, then the records in order,
 // each an fma. Adjacent columns (2k, 2k+1) of a row travel as one packed pair.
-template <bool KDA>
+template <bool KDA, bool B4>
 __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -815,13 +838,16 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
     // the 32 accumulator pairs.
     const float* lam = at<float>(sm, L.lam_b) + 20 * qq;
     const float* p0b = P_b + 20 * qq;
-    const int8_t* cb = at<int8_t>(sm, L.codes) + 16 * qq;
+    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
       const float s_i = sg[i];
+      uint32_t cw[4];
+      code_words<B4>(cb + i * row_bytes<B4>(), cw);
       float f[16];
-      codes16_to_float(*reinterpret_cast<const int4*>(cb + i * kD), f);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) f[t] = code_at<B4>(cw, t);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float2 l2 = *reinterpret_cast<const float2*>(lam + 2 * k);
@@ -991,6 +1017,7 @@ __device__ __forceinline__ void column_quads(const float* S, float* colpart) {
 }
 
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
+template <bool B4>
 __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1121,7 +1148,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   {
     float g[16];
     load16(tl.gsc_b + 20 * qq, g);
-    int8_t* cbase = p.codes + s * (kD * kD) + 16 * qq;
+    int8_t* cbase = p.codes + s * (kD * row_bytes<B4>()) + (B4 ? 8 : 16) * qq;
     int roff[4];
     row_offsets(4 * w + r, qq, roff);
     float t[4][16], mx[4];
@@ -1167,18 +1194,30 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     for (int pp = 0; pp < 4; ++pp) {
       const float hh = __shfl_sync(0xffffffffu, hown, (lane & ~7) | ((pp >> 1) | ((pp & 1) << 1)));
       const int i = 32 * pp + 4 * w + r;
-      // Round t*h to the nearest integer, ties to even: |t*h| <= 127(1+2^-24)^2
-      // < 127.5, so adding 1.5 * 2^23 leaves the integer, in [-127, 127], in
-      // the low mantissa bits (two's complement), and no clamp is needed.
+      // Round t*h to the nearest integer, ties to even: |t*h| <= q(1+2^-24)^2 <
+      // q + 1/2 (q = 127 or 7), so adding 1.5 * 2^23 leaves the integer, in
+      // [-q, q], in the low mantissa bits (two's complement), and no clamp is
+      // needed. For 4-bit codes the added constant carries the +8 bias too, so
+      // the low nibble is c + 8 (1..15).
       uint32_t rb[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[pp][e], hh), 12582912.0f));
-      uint32_t wd[4];
+      for (int e = 0; e < 16; ++e)
+        rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[pp][e], hh), B4 ? 12582920.0f : 12582912.0f));
+      if (B4) {
+        uint32_t v[8];  // byte 0 of v[k]: codes 2k (low nibble) and 2k + 1
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        wd[q4] = __byte_perm(__byte_perm(rb[4 * q4], rb[4 * q4 + 1], 0x0040u),
-                             __byte_perm(rb[4 * q4 + 2], rb[4 * q4 + 3], 0x0040u), 0x5410u);
-      *reinterpret_cast<int4*>(cbase + i * kD) = make_int4((int)wd[0], (int)wd[1], (int)wd[2], (int)wd[3]);
+        for (int k = 0; k < 8; ++k) v[k] = rb[2 * k] | (rb[2 * k + 1] << 4);
+        const uint32_t w0 = __byte_perm(__byte_perm(v[0], v[1], 0x0040u), __byte_perm(v[2], v[3], 0x0040u), 0x5410u);
+        const uint32_t w1 = __byte_perm(__byte_perm(v[4], v[5], 0x0040u), __byte_perm(v[6], v[7], 0x0040u), 0x5410u);
+        *reinterpret_cast<uint2*>(cbase + i * row_bytes<B4>()) = make_uint2(w0, w1);
+      } else {
+        uint32_t wd[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          wd[q4] = __byte_perm(__byte_perm(rb[4 * q4], rb[4 * q4 + 1], 0x0040u),
+                               __byte_perm(rb[4 * q4 + 2], rb[4 * q4 + 3], 0x0040u), 0x5410u);
+        *reinterpret_cast<int4*>(cbase + i * kD) = make_int4((int)wd[0], (int)wd[1], (int)wd[2], (int)wd[3]);
+      }
     }
   }
   // F6: the buffer is emptied.
@@ -1259,7 +1298,7 @@ __host__ __device__ inline int append_slots(int W, int phase) { return (phase >=
 
 // KPRE (the phase is stated): the record keys are not staged; each lane group
 // reads its record's key block into registers before the staging wait.
-template <bool KDA, bool KPRE>
+template <bool KDA, bool KPRE, bool B4>
 __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1282,12 +1321,12 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, !KPRE, slots);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false, KPRE>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 128, false, KPRE, B4>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
-template <bool KDA>
+template <bool KDA, bool B4>
 __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1303,24 +1342,24 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   if (n0 < 0) return;
   const int n = n0 + 1;
   if (n < p.W) {
-    append_compute<KDA, 256, false, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+    append_compute<KDA, 256, false, false, B4>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  append_compute<KDA, 256, true, false>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 256, true, false, B4>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile(p, s, S, tl);
+  boundary_from_tile<B4>(p, s, S, tl);
 }
 
 // Fold with the records held (any count 0..W): lq_fold.
-template <bool KDA>
+template <bool KDA, bool B4>
 __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1334,16 +1373,16 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile(p, s, S, tl);
+  boundary_from_tile<B4>(p, s, S, tl);
 }
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
-template <bool KDA>
+template <bool KDA, bool B4>
 __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1359,7 +1398,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
@@ -1371,6 +1410,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
 }
 
 // Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
+template <bool B4>
 __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
@@ -1398,7 +1438,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile(p, s, S, tl);
+  boundary_from_tile<B4>(p, s, S, tl);
 }
 
 // ---------------------------------------------------------------------------
@@ -1406,7 +1446,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
 
 static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile) {
   Params q = p;
-  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold);
+  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits);
   q.r1 = tile ? region1_bytes(q.st) : q.st.end;
   return q;
 }
@@ -1424,32 +1464,42 @@ static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, 
 
 cudaError_t launch_init(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, 0, 0, false, false, true);
-  return launch(k_init, q, smem_of(q, true), st);
+  return p.bits == 4 ? launch(k_init<true>, q, smem_of(q, true), st) : launch(k_init<false>, q, smem_of(q, true), st);
 }
+
+// Kernel K<KDA, B4> for this configuration's decay form and code width.
+#define LQ_PICK2(K, q) \
+  ((q).kda ? ((q).bits == 4 ? K<true, true> : K<true, false>) : ((q).bits == 4 ? K<false, true> : K<false, false>))
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const int slots = append_slots(p.W, p.phase);
   const bool stated = p.phase >= 0 && p.phase < p.W;
   const Params q = with_layout(p, slots, stated ? 0 : slots, true, false, false);
   const int smem = smem_of(q, false);
-  if (stated)
-    return p.kda ? launch(k_append<true, true>, q, smem, st, 128) : launch(k_append<false, true>, q, smem, st, 128);
-  return p.kda ? launch(k_append<true, false>, q, smem, st, 128) : launch(k_append<false, false>, q, smem, st, 128);
+  const bool b4 = p.bits == 4;
+  if (stated) {
+    if (p.kda) return b4 ? launch(k_append<true, true, true>, q, smem, st, 128) : launch(k_append<true, true, false>, q, smem, st, 128);
+    return b4 ? launch(k_append<false, true, true>, q, smem, st, 128) : launch(k_append<false, true, false>, q, smem, st, 128);
+  }
+  if (p.kda) return b4 ? launch(k_append<true, false, true>, q, smem, st, 128) : launch(k_append<true, false, false>, q, smem, st, 128);
+  return b4 ? launch(k_append<false, false, true>, q, smem, st, 128) : launch(k_append<false, false, false>, q, smem, st, 128);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, p.W, p.W, true, true, true);
-  return p.kda ? launch(k_step<true>, q, smem_of(q, true), st) : launch(k_step<false>, q, smem_of(q, true), st);
+  return launch(LQ_PICK2(k_step, q), q, smem_of(q, true), st);
 }
 
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, p.W, p.W, false, true, true);
-  return p.kda ? launch(k_fold<true>, q, smem_of(q, true), st) : launch(k_fold<false>, q, smem_of(q, true), st);
+  return launch(LQ_PICK2(k_fold, q), q, smem_of(q, true), st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, p.W, p.W, false, true, true);
-  return p.kda ? launch(k_export<true>, q, smem_of(q, true), st) : launch(k_export<false>, q, smem_of(q, true), st);
+  return launch(LQ_PICK2(k_export, q), q, smem_of(q, true), st);
 }
+
+#undef LQ_PICK2
 
 }  // namespace lqi

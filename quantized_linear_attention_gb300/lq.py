@@ -36,7 +36,7 @@ EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", 
 class Config(ctypes.Structure):
     _fields_ = [("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("n_comp", ctypes.c_int32), ("decay_per_key", ctypes.c_int32), ("smooth", ctypes.c_int32),
-                ("lambda_floor", ctypes.c_float)]
+                ("lambda_floor", ctypes.c_float), ("code_bits", ctypes.c_int32)]
 
 
 class Layout(ctypes.Structure):
@@ -103,8 +103,8 @@ def _check(rc):
         raise LQError(rc, last_error())
 
 
-def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128) -> Config:
-    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor)
+def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128, code_bits=8) -> Config:
+    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor, code_bits)
 
 
 def default_config() -> Config:
@@ -213,7 +213,9 @@ def clear_status(state, stream=None):
 
 
 def state_views(cfg: Config, state, n_states: int) -> dict:
-    """Typed torch views of the planes of a state buffer (no copy), per ``lq_layout``."""
+    """Typed torch views of the planes of a state buffer (no copy), per ``lq_layout``. With
+    4-bit codes, "codes" is the packed plane: uint8 [N][d_v][d_k / 2], two codes per
+    byte (low nibble first), each stored as c + 8."""
     import torch
 
     L = layout(cfg, n_states)
@@ -225,7 +227,8 @@ def state_views(cfg: Config, state, n_states: int) -> dict:
 
     return {
         "counts": view(L.counts, N, torch.int32, (N,)),
-        "codes": view(L.codes, N * D * D, torch.int8, (N, D, D)),
+        "codes": (view(L.codes, N * D * D, torch.int8, (N, D, D)) if cfg.code_bits == 8 else
+                  view(L.codes, N * D * D // 2, torch.uint8, (N, D, D // 2))),
         "sigma": view(L.sigma, N * D, torch.float32, (N, D)),
         "lambda": view(L.lambda_, N * D, torch.float32, (N, D)),
         "comp_id": view(L.comp_id, N * L.comp_id_stride, torch.int32, (N, L.comp_id_stride))[:, :C],

@@ -16,10 +16,24 @@ def to_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(DEV, non_blocking=False)
 
 
+def unpack_codes(codes):
+    """Code values (int8) from the codes plane: as is for 8-bit codes; for 4-bit
+    codes, two per byte (low nibble first), each stored as c + 8."""
+    if codes.dtype == np.int8:
+        return codes
+    lo = (codes & 0x0F).astype(np.int16) - 8
+    hi = (codes >> 4).astype(np.int16) - 8
+    out = np.empty(codes.shape[:-1] + (2 * codes.shape[-1],), np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
 class GpuState:
-    def __init__(self, n, W=16, C=4, kda=False, smooth=True, lambda_floor=1e-6):
+    def __init__(self, n, W=16, C=4, kda=False, smooth=True, lambda_floor=1e-6, code_bits=8):
         self.n, self.W, self.C, self.kda = n, W, C, kda
-        self.cfg = lq.config(window=W, n_comp=C, kda=kda, smooth=smooth, lambda_floor=lambda_floor)
+        self.cfg = lq.config(window=W, n_comp=C, kda=kda, smooth=smooth, lambda_floor=lambda_floor,
+                             code_bits=code_bits)
         self.state = lq.alloc_state(self.cfg, n, DEV)
         self.views = lq.state_views(self.cfg, self.state, n)
         self.o = torch.empty((n, 128), dtype=torch.float32, device=DEV)
@@ -48,7 +62,7 @@ class GpuState:
     def boundary(self, idx=None):
         idx = slice(None) if idx is None else torch.as_tensor(idx, device=DEV)
         v = self.views
-        return dict(codes=v["codes"][idx].cpu().numpy(), sigma=v["sigma"][idx].cpu().numpy(),
+        return dict(codes=unpack_codes(v["codes"][idx].cpu().numpy()), sigma=v["sigma"][idx].cpu().numpy(),
                     lam=v["lambda"][idx].cpu().numpy(), comp_id=v["comp_id"][idx].cpu().numpy(),
                     comp_line=v["comp_line"][idx].cpu().numpy(), count=v["counts"][idx].cpu().numpy())
 
@@ -94,7 +108,7 @@ def compare_boundary(g, ref: OracleState, ref_idx, diags=None, tally: Tally | No
 
 
 def run_and_compare(wl: wlm.Workload, n_tokens: int, sample=None, phase_mode="stated", chunk=64, W=None, C=None,
-                    smooth=True, tally=None, use_append_fold=False):
+                    smooth=True, tally=None, use_append_fold=False, code_bits=8):
     """Free-running decode of n_tokens for all wl.n_states head-states on the GPU; the
     oracle follows the sampled states. Compares o every token, records every
     token, boundaries after every fold. Returns the Tally."""
@@ -104,9 +118,9 @@ def run_and_compare(wl: wlm.Workload, n_tokens: int, sample=None, phase_mode="st
     sample = list(range(N)) if sample is None else list(sample)
     tally = tally or Tally()
     S0, _ = wlm.initial_state(wl)
-    gpu = GpuState(N, W=W, C=C, kda=wl.kda, smooth=smooth)
+    gpu = GpuState(N, W=W, C=C, kda=wl.kda, smooth=smooth, code_bits=code_bits)
     gpu.init(S0)
-    ref = OracleState(len(sample), W=W, C=C, decay_per_key=wl.kda, smooth=smooth)
+    ref = OracleState(len(sample), W=W, C=C, decay_per_key=wl.kda, smooth=smooth, code_bits=code_bits)
     d0 = [FoldDiag(128, 128) for _ in sample]
     ref.init(None if S0 is None else S0[sample], diags=d0)
     sidx = torch.as_tensor(sample, device=DEV)

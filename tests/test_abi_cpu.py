@@ -52,6 +52,18 @@ def test_pin8_boundary_bytes_per_element(L):
     assert round(4 / per_elem, 1) == g["boundary_storage_reduction"]
 
 
+def test_boundary_bytes_with_4bit_codes(L):
+    """4-bit codes (LeapQuant §4 also evaluates 4-bit states): two codes per byte,
+    so the boundary takes 8192 + 512 + 512 + 4C + 512C bytes, 0.69 per element."""
+    lay = lq.layout(lq.config(code_bits=4), 1)
+    assert lay.boundary_bytes_per_state == 8192 + 512 + 512 + 4 * 4 + 4 * 512 == 11280
+    assert round(lay.boundary_bytes_per_state / (128 * 128), 2) == 0.69
+    l8 = lq.layout(lq.config(), 1000)
+    l4 = lq.layout(lq.config(code_bits=4), 1000)
+    assert l8.total_bytes - l4.total_bytes == 1000 * 8192
+    assert l4.sigma - l4.codes == 1000 * 8192
+
+
 @pytest.mark.parametrize("kda", [False, True])
 @pytest.mark.parametrize("n", [1, 3, 1024, 16384])
 def test_layout_planes(L, n, kda):
@@ -77,7 +89,8 @@ def test_layout_planes(L, n, kda):
     ("d_k", 64, lq.ERR_UNSUPPORTED), ("d_v", 256, lq.ERR_UNSUPPORTED), ("window", 0, lq.ERR_UNSUPPORTED),
     ("window", 33, lq.ERR_UNSUPPORTED), ("n_comp", 9, lq.ERR_UNSUPPORTED), ("n_comp", -1, lq.ERR_UNSUPPORTED),
     ("decay_per_key", 2, lq.ERR_INVALID_ARG), ("smooth", 3, lq.ERR_INVALID_ARG),
-    ("lambda_floor", 0.0, lq.ERR_INVALID_ARG), ("lambda_floor", float("inf"), lq.ERR_INVALID_ARG)])
+    ("lambda_floor", 0.0, lq.ERR_INVALID_ARG), ("lambda_floor", float("inf"), lq.ERR_INVALID_ARG),
+    ("code_bits", 6, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG), ("code_bits", 0, lq.ERR_INVALID_ARG)])
 def test_invalid_config_rejected(L, field, value, code):
     cfg = lq.default_config()
     setattr(cfg, field, value)
