@@ -1181,11 +1181,13 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     }
     float m1 = fmaxf(b1 ? m2[1] : m2[0], __shfl_xor_sync(0xffffffffu, b1 ? m2[0] : m2[1], 2));
     m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
-    // sigma = m / 127 and the reciprocal h = 127 / m, once per row; zero row: 0, 0.
+    // sigma = m / q and the reciprocal h = q / m, once per row (q = 127 for
+    // 8-bit codes, 7 for 4-bit ones); zero row: 0, 0.
+    constexpr float q = B4 ? 7.0f : 127.0f;
     float sgm = 0.0f, hown = 0.0f;
     if (m1 != 0.0f) {
-      sgm = __fdiv_rn(m1, 127.0f);
-      hown = __fdiv_rn(127.0f, m1);
+      sgm = __fdiv_rn(m1, q);
+      hown = __fdiv_rn(q, m1);
     }
     const int pp_own = 2 * (qq & 1) + ((qq >> 1) & 1);
     if ((qq & 4) == 0) p.sigma[s * kD + 32 * pp_own + 4 * w + r] = sgm;
