@@ -57,6 +57,10 @@ typedef struct {
   float lambda_floor;    /* positive floor of the smoothing scales               */
   int32_t code_bits;     /* code width b (2..8): codes in [-qmax, qmax],         */
                          /* qmax = 2^(b-1) - 1 ([LQ] §4: 8-, 6- and 4-bit states) */
+  int32_t comp_fit;      /* 0: compensators are outlier lines (id + line);       */
+                         /* s > 0: rank-one factors (a, b) fitted by s sweeps of */
+                         /* power iteration from the longest row ([RN4] "Where   */
+                         /* the time goes"; [LQ] App. B.3 "fitting new factors") */
 } orc_cfg;
 
 /* Batch storage; every array holds n_states consecutive per-state blocks. */
@@ -84,6 +88,8 @@ typedef struct {
 enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_WINDOW_FULL = -3 };
 
 static int line_len(const orc_cfg* c) { return c->dk > c->dv ? c->dk : c->dv; }
+/* floats per compensator: one line, or the factor pair a (d_v) then b (d_k) */
+static int comp_len(const orc_cfg* c) { return c->comp_fit > 0 ? c->dv + c->dk : line_len(c); }
 static int alpha_len(const orc_cfg* c) { return c->decay_per_key ? c->dk : 1; }
 
 static int is_block_size(int d) {
@@ -152,7 +158,7 @@ static void decay_products(int n, int alen, const float* alphas, float* P) {
 
 static float pj(const float* Pm, int alen, int j) { return alen == 1 ? Pm[0] : Pm[j]; }
 
-/* Expand compensator c into (a, b): a has length dv, b has length dk. */
+/* Expand an outlier-line compensator into (a, b): a has length dv, b has length dk. */
 static void expand_comp(const orc_cfg* cfg, int32_t id, const float* line, float* a, float* b) {
   for (int i = 0; i < cfg->dv; ++i) a[i] = 0.0f;
   for (int j = 0; j < cfg->dk; ++j) b[j] = 0.0f;
@@ -178,13 +184,24 @@ static orc_view view_of(const orc_cfg* c, const orc_batch* b, int64_t s) {
   v.sigma = b->sigma ? b->sigma + s * dv : NULL;
   v.lambda = b->lambda ? b->lambda + s * dk : NULL;
   v.comp_id = b->comp_id ? b->comp_id + s * C : NULL;
-  v.comp_line = b->comp_line ? b->comp_line + s * C * (size_t)line_len(c) : NULL;
+  v.comp_line = b->comp_line ? b->comp_line + s * C * (size_t)comp_len(c) : NULL;
   v.B = b->B ? b->B + s * dv * dk : NULL;
   v.rec_k = b->rec_k + s * W * dk;
   v.rec_u = b->rec_u + s * W * dv;
   v.rec_alpha = b->rec_alpha + s * W * (size_t)alpha_len(c);
   v.count = b->count + s;
   return v;
+}
+
+/* Compensator c of a head-state as its rank-one term a_c b_c^T. */
+static void comp_vectors(const orc_cfg* cfg, orc_view st, int c, float* a, float* b) {
+  const float* line = st.comp_line + (size_t)c * comp_len(cfg);
+  if (cfg->comp_fit > 0) {
+    memcpy(a, line, sizeof(float) * (size_t)cfg->dv);
+    memcpy(b, line + cfg->dv, sizeof(float) * (size_t)cfg->dk);
+  } else {
+    expand_comp(cfg, st.comp_id[c], line, a, b);
+  }
 }
 
 /*
@@ -238,7 +255,7 @@ static int append_one(const orc_cfg* cfg, orc_view st, const float* q, const flo
   /* A3: compensators are records at window position 0 ([LQ] §3.3: they share
    * the real-token update path and are processed before the window's tokens). */
   for (int c = 0; c < cfg->C; ++c) {
-    expand_comp(cfg, st.comp_id[c], st.comp_line + (size_t)c * line_len(cfg), ca, cb);
+    comp_vectors(cfg, st, c, ca, cb);
     float e = orc_dot(dk, cb, 1, y, 1);
     for (int i = 0; i < dv; ++i) acc[i] = fmaf(ca[i], e, acc[i]);
   }
@@ -269,7 +286,7 @@ static int append_one(const orc_cfg* cfg, orc_view st, const float* q, const flo
       o[i] = s;
     }
     for (int c = 0; c < cfg->C; ++c) {
-      expand_comp(cfg, st.comp_id[c], st.comp_line + (size_t)c * line_len(cfg), ca, cb);
+      comp_vectors(cfg, st, c, ca, cb);
       double e = 0.0;
       for (int j = 0; j < dk; ++j) e += (double)cb[j] * w[j];
       for (int i = 0; i < dv; ++i) o[i] += (double)ca[i] * e;
@@ -312,6 +329,61 @@ static int append_one(const orc_cfg* cfg, orc_view st, const float* q, const flo
  * floor, fixed within the next window; the inverse restores key coordinates
  * after dequantization. Quantizer: symmetric int8, per-row absmax.
  */
+/* b <- b / ||b|| (through one reciprocal, ||b|| = sqrt(dot(b, b))); a zero b stays zero. */
+static void normalize(int d, float* b) {
+  const float nrm = sqrtf(orc_dot(d, b, 1, b, 1));
+  if (nrm > 0.0f) {
+    const float inv = 1.0f / nrm;
+    for (int j = 0; j < d; ++j) b[j] = b[j] * inv;
+  }
+}
+
+/*
+ * F2, fitted-factor reading of the compensators ([LQ] §3.3: dominant state
+ * components kept as high-precision rank-one terms; App. B.3: the state is
+ * reconstructed "before fitting new factors"; [RN4] "Where the time goes": four
+ * compensators found one at a time, eight sweeps each, starting from the
+ * longest row). For c = 0..C-1, on the residual R:
+ *   b = the longest row of R (largest squared length, ties to the smallest index);
+ *   s sweeps of: normalize b; a = R b; b = R^T a;
+ *   normalize b; a = R b; the compensator is (a, b);
+ *   deflate: R_ij = fma(-a_i, b_j, R_ij).
+ * Every product sum is a dot in the fixed order; the compensator id records the
+ * starting row.
+ */
+static void fit_factors(const orc_cfg* cfg, float* R, orc_view st) {
+  const int dk = cfg->dk, dv = cfg->dv;
+  float* a = (float*)malloc(sizeof(float) * dv);
+  float* b = (float*)malloc(sizeof(float) * dk);
+  for (int c = 0; c < cfg->C; ++c) {
+    int best = 0;
+    float bestv = orc_dot(dk, R, 1, R, 1);
+    for (int i = 1; i < dv; ++i) {
+      const float sc = orc_dot(dk, R + (size_t)i * dk, 1, R + (size_t)i * dk, 1);
+      if (sc > bestv) {
+        bestv = sc;
+        best = i;
+      }
+    }
+    memcpy(b, R + (size_t)best * dk, sizeof(float) * dk);
+    for (int sweep = 0; sweep < cfg->comp_fit; ++sweep) {
+      normalize(dk, b);
+      for (int i = 0; i < dv; ++i) a[i] = orc_dot(dk, R + (size_t)i * dk, 1, b, 1);
+      for (int j = 0; j < dk; ++j) b[j] = orc_dot(dv, R + j, dk, a, 1);
+    }
+    normalize(dk, b);
+    for (int i = 0; i < dv; ++i) a[i] = orc_dot(dk, R + (size_t)i * dk, 1, b, 1);
+    float* out = st.comp_line + (size_t)c * comp_len(cfg);
+    memcpy(out, a, sizeof(float) * dv);
+    memcpy(out + dv, b, sizeof(float) * dk);
+    st.comp_id[c] = best;
+    for (int i = 0; i < dv; ++i)
+      for (int j = 0; j < dk; ++j) R[(size_t)i * dk + j] = fmaf(-a[i], b[j], R[(size_t)i * dk + j]);
+  }
+  free(a);
+  free(b);
+}
+
 static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st, orc_diag* dg) {
   const int dk = cfg->dk, dv = cfg->dv, L = line_len(cfg);
   float* R = (float*)malloc(sizeof(float) * (size_t)dv * dk);
@@ -320,34 +392,38 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
   float* g = (float*)malloc(sizeof(float) * dk);
   memcpy(R, S, sizeof(float) * (size_t)dv * dk);
 
-  /* F2: C greedy rounds. Score of a line = its squared L2 length
-   * (the "longest" line); ties go to the smallest id, rows before columns.
-   * The chosen line is copied exactly and zeroed in the residual (deflation). */
-  for (int c = 0; c < cfg->C; ++c) {
-    for (int i = 0; i < dv; ++i) rho[i] = orc_dot(dk, R + (size_t)i * dk, 1, R + (size_t)i * dk, 1);
-    for (int j = 0; j < dk; ++j) gam[j] = orc_dot(dv, R + j, dk, R + j, dk);
-    int best = 0;
-    float bestv = rho[0];
-    for (int id = 1; id < dv + dk; ++id) {
-      float sc = id < dv ? rho[id] : gam[id - dv];
-      if (sc > bestv) {
-        bestv = sc;
-        best = id;
+  if (cfg->comp_fit > 0) {
+    fit_factors(cfg, R, st);
+  } else {
+    /* F2: C greedy rounds. Score of a line = its squared L2 length
+     * (the "longest" line); ties go to the smallest id, rows before columns.
+     * The chosen line is copied exactly and zeroed in the residual (deflation). */
+    for (int c = 0; c < cfg->C; ++c) {
+      for (int i = 0; i < dv; ++i) rho[i] = orc_dot(dk, R + (size_t)i * dk, 1, R + (size_t)i * dk, 1);
+      for (int j = 0; j < dk; ++j) gam[j] = orc_dot(dv, R + j, dk, R + j, dk);
+      int best = 0;
+      float bestv = rho[0];
+      for (int id = 1; id < dv + dk; ++id) {
+        float sc = id < dv ? rho[id] : gam[id - dv];
+        if (sc > bestv) {
+          bestv = sc;
+          best = id;
+        }
       }
-    }
-    float* line = st.comp_line + (size_t)c * L;
-    for (int e = 0; e < L; ++e) line[e] = 0.0f;
-    st.comp_id[c] = best;
-    if (best < dv) {
-      for (int j = 0; j < dk; ++j) {
-        line[j] = R[(size_t)best * dk + j];
-        R[(size_t)best * dk + j] = 0.0f;
-      }
-    } else {
-      int j = best - dv;
-      for (int i = 0; i < dv; ++i) {
-        line[i] = R[(size_t)i * dk + j];
-        R[(size_t)i * dk + j] = 0.0f;
+      float* line = st.comp_line + (size_t)c * L;
+      for (int e = 0; e < L; ++e) line[e] = 0.0f;
+      st.comp_id[c] = best;
+      if (best < dv) {
+        for (int j = 0; j < dk; ++j) {
+          line[j] = R[(size_t)best * dk + j];
+          R[(size_t)best * dk + j] = 0.0f;
+        }
+      } else {
+        int j = best - dv;
+        for (int i = 0; i < dv; ++i) {
+          line[i] = R[(size_t)i * dk + j];
+          R[(size_t)i * dk + j] = 0.0f;
+        }
       }
     }
   }
@@ -420,8 +496,7 @@ static void reconstruct(const orc_cfg* cfg, orc_view st, float* S) {
     for (int j = 0; j < dk; ++j)
       kd[(size_t)(m - 1) * dk + j] = pj(P + (size_t)m * alen, alen, j) * st.rec_k[(size_t)(m - 1) * dk + j];
   for (int c = 0; c < C; ++c) {
-    expand_comp(cfg, st.comp_id[c], st.comp_line + (size_t)c * line_len(cfg), ca + (size_t)c * dv,
-                bd + (size_t)c * dk);
+    comp_vectors(cfg, st, c, ca + (size_t)c * dv, bd + (size_t)c * dk);
     for (int j = 0; j < dk; ++j) bd[(size_t)c * dk + j] = pj(P0, alen, j) * bd[(size_t)c * dk + j];
   }
   for (int i = 0; i < dv; ++i) {
@@ -464,6 +539,7 @@ static int cfg_ok(const orc_cfg* c) {
   if (!c->quantize && c->C != 0) return 0;
   if (!(c->lambda_floor > 0.0f)) return 0;
   if (c->code_bits < 2 || c->code_bits > 8) return 0;
+  if (c->comp_fit < 0 || c->comp_fit > 64) return 0;
   return 1;
 }
 

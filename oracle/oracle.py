@@ -30,6 +30,7 @@ class Cfg(ctypes.Structure):
         ("quantize", ctypes.c_int32),
         ("lambda_floor", ctypes.c_float),
         ("code_bits", ctypes.c_int32),
+        ("comp_fit", ctypes.c_int32),
     ]
 
 
@@ -119,19 +120,22 @@ class OracleState:
     """Boundary + record buffer for ``n_states`` head-states, as numpy arrays."""
 
     def __init__(self, n_states, dk=128, dv=128, W=16, C=4, decay_per_key=False, smooth=True, quantize=True,
-                 lambda_floor=1e-6, code_bits=8):
+                 lambda_floor=1e-6, code_bits=8, comp_fit=0):
         self.n, self.dk, self.dv, self.W, self.C = int(n_states), int(dk), int(dv), int(W), int(C)
         self.kda = bool(decay_per_key)
         self.code_bits = int(code_bits)
+        self.comp_fit = int(comp_fit)
         self.cfg = Cfg(self.dk, self.dv, self.W, self.C, int(decay_per_key), int(smooth), int(quantize),
-                       float(lambda_floor), self.code_bits)
+                       float(lambda_floor), self.code_bits, self.comp_fit)
         N, L = self.n, max(self.dk, self.dv)
         alen = self.dk if self.kda else 1
         self.codes = np.zeros((N, self.dv, self.dk), np.int8)
         self.sigma = np.zeros((N, self.dv), np.float32)
         self.lam = np.ones((N, self.dk), np.float32)
         self.comp_id = np.zeros((N, max(self.C, 1)), np.int32)
-        self.comp_line = np.zeros((N, max(self.C, 1), L), np.float32)
+        # one line per compensator, or with fitted factors a (d_v) then b (d_k)
+        clen = self.dv + self.dk if self.comp_fit > 0 else L
+        self.comp_line = np.zeros((N, max(self.C, 1), clen), np.float32)
         self.B = np.zeros((N, self.dv, self.dk), np.float32) if not quantize else None
         self.rec_k = np.zeros((N, self.W, self.dk), np.float32)
         self.rec_u = np.zeros((N, self.W, self.dv), np.float32)
@@ -208,6 +212,10 @@ class OracleState:
         B = (self.sigma[s].astype(np.float64)[:, None] * self.codes[s].astype(np.float64)
              * self.lam[s].astype(np.float64)[None, :])
         for c in range(self.C):
+            if self.comp_fit > 0:
+                line = self.comp_line[s, c].astype(np.float64)
+                B += np.outer(line[:self.dv], line[self.dv:])
+                continue
             cid = int(self.comp_id[s, c])
             if cid < self.dv:
                 B[cid, :] += self.comp_line[s, c, :self.dk]
