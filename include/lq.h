@@ -73,6 +73,10 @@ typedef struct {
   float lambda_floor;    /* positive floor of the smoothing scales (default 1e-6)           */
   int32_t code_bits;     /* code width: 8 (default) or 4 ([LQ] §4 also evaluates 6- and      */
                          /* 4-bit states); codes in [-q, q], q = 2^(bits-1) - 1              */
+  int32_t comp_fit;      /* 0 (default): a compensator is an outlier line, kept exactly;     */
+                         /* 1..32: a rank-one factor a b^T fitted to the residual by that   */
+                         /* many power-iteration sweeps from the longest row ([LQ] §3.3,    */
+                         /* App. B.3 "fitting new factors"; [RN4] "Where the time goes")    */
 } lq_config;
 
 /*
@@ -86,7 +90,8 @@ typedef struct {
  *   sigma    fp32    [s][d_v]                  quantization step of each value row
  *   lambda   fp32    [s][d_k]                  smoothing scale of each key channel
  *   comp_id  int32   [s][comp_id_stride]       id < d_v: row id; else column id - d_v
- *   comp_line fp32   [s][C][128]               the compensator line
+ *   comp_line fp32   [s][C][128]               the compensator line, or with comp_fit > 0
+ *            fp32    [s][C][256]               the factor pair: a (d_v), then unit b (d_k)
  *   rec_k    fp32    [s][W][d_k]               record keys, slot m-1 holds record m
  *   rec_u    fp32    [s][W][d_v]               record corrections u_m
  *   rec_alpha fp32   [s][alpha_stride]         GDN: W scalars; KDA: [W][d_k]

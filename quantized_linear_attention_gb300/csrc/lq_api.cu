@@ -54,6 +54,8 @@ int check_cfg(const lq_config* c) {
   if (c->smooth != 0 && c->smooth != 1) return fail(LQ_ERR_INVALID_ARG, "smooth must be 0 or 1 (got %d)", c->smooth);
   if (!(c->lambda_floor > 0.0f) || !std::isfinite(c->lambda_floor))
     return fail(LQ_ERR_INVALID_ARG, "lambda_floor must be finite and > 0");
+  if (c->comp_fit < 0 || c->comp_fit > 32)
+    return fail(LQ_ERR_INVALID_ARG, "comp_fit must be 0..32 (got %d)", c->comp_fit);
   if (c->code_bits != 8 && c->code_bits != 4) {
     if (c->code_bits >= 2 && c->code_bits <= 7)
       return fail(LQ_ERR_UNSUPPORTED, "code_bits %d: this build runs 8- and 4-bit codes", c->code_bits);
@@ -68,7 +70,7 @@ int check_n(int64_t n) {
 }
 
 uint64_t cfg_hash(const lq_config* c, int64_t n) {
-  const int64_t f[8] = {c->d_k, c->d_v, c->window, c->n_comp, c->decay_per_key, c->smooth, c->code_bits, n};
+  const int64_t f[9] = {c->d_k, c->d_v, c->window, c->n_comp, c->decay_per_key, c->smooth, c->code_bits, c->comp_fit, n};
   uint32_t fl;
   std::memcpy(&fl, &c->lambda_floor, 4);
   uint64_t h = 1469598103934665603ull;  // FNV-1a
@@ -105,7 +107,7 @@ void make_layout(const lq_config* c, int64_t n, lq_layout_t* L) {
   L->comp_id = off;
   off = align256(off + 4 * N * (size_t)L->comp_id_stride);
   L->comp_line = off;
-  off = align256(off + 4 * N * C * D);
+  off = align256(off + 4 * N * C * D * (c->comp_fit > 0 ? 2 : 1));
   L->rec_k = off;
   off = align256(off + 4 * N * W * D);
   L->rec_u = off;
@@ -113,7 +115,8 @@ void make_layout(const lq_config* c, int64_t n, lq_layout_t* L) {
   L->rec_alpha = off;
   off = align256(off + 4 * N * (size_t)L->alpha_stride);
   L->total_bytes = off;
-  L->boundary_bytes_per_state = (int64_t)(D * D * (size_t)c->code_bits / 8 + 4 * D + 4 * D + 4 * C + 4 * C * D);
+  L->boundary_bytes_per_state =
+      (int64_t)(D * D * (size_t)c->code_bits / 8 + 4 * D + 4 * D + 4 * C + 4 * C * D * (c->comp_fit > 0 ? 2 : 1));
 }
 
 int current_device(int* dev) {
@@ -169,6 +172,7 @@ Params make_params(const lq_config* c, void* state, int64_t n) {
   p.kda = c->decay_per_key;
   p.smooth = c->smooth;
   p.bits = c->code_bits;
+  p.comp_fit = c->comp_fit;
   p.lambda_floor = c->lambda_floor;
   p.phase = -1;
   p.n_states = n;
@@ -235,6 +239,7 @@ void lq_config_default(lq_config* cfg) {
   cfg->decay_per_key = 0;
   cfg->smooth = 1;
   cfg->code_bits = 8;
+  cfg->comp_fit = 0;
   cfg->lambda_floor = 1e-6f;
 }
 

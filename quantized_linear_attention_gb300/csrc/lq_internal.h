@@ -43,7 +43,8 @@ struct Stage {
 // Everything a kernel needs, passed by value.
 struct Params {
   int W, C, kda, smooth;
-  int bits;  // code width: 8 or 4
+  int bits;      // code width: 8 or 4
+  int comp_fit;  // 0: outlier-line compensators; s > 0: factors fitted by s sweeps
   float lambda_floor;
   int phase;  // expected record count before the call, or -1
   int64_t n_states;

@@ -289,7 +289,7 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 // when the keys travel in registers). The token's q, k, v (and alpha) are read
 // into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
-                                              bool append, bool fold, int bits) {
+                                              bool append, bool fold, int bits, int comp_fit) {
   Stage L;
   int o = 0;
   auto take = [&](int bytes) {
@@ -302,7 +302,7 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.sigma = take(4 * kD);
   L.lambda = take(4 * kD);
   L.comp_id = take(4 * comp_id_stride);
-  L.comp_line = take(4 * kD * C);
+  L.comp_line = take(4 * kD * C * (comp_fit > 0 ? 2 : 1));
   L.rec_k = take(4 * kD * slots_k);
   L.rec_u = take(4 * kD * slots_u);
   L.rec_alpha = take(kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
@@ -373,7 +373,8 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
   const uint32_t rec = 4u * kD * (uint32_t)n0;
   const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
   const uint32_t code_bytes = (uint32_t)(kD * kD * p.bits / 8);
-  uint32_t bytes = code_bytes + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * kD * (uint32_t)p.C + rec;
+  const uint32_t comp_floats = (uint32_t)(kD * p.C * (p.comp_fit > 0 ? 2 : 1));
+  uint32_t bytes = code_bytes + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * comp_floats + rec;
   if (!p.kda || n0 > 0) bytes += alpha_bytes;
   if (stage_k) bytes += rec;
   mbar_expect_tx(bar, bytes);
@@ -381,7 +382,7 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
   bulk_g2s(sm + L.sigma, p.sigma + s * kD, 4 * kD, bar);
   bulk_g2s(sm + L.lambda, p.lambda + s * kD, 4 * kD, bar);
   bulk_g2s(sm + L.comp_id, p.comp_id + s * p.comp_id_stride, 4u * (uint32_t)p.comp_id_stride, bar);
-  if (p.C > 0) bulk_g2s(sm + L.comp_line, p.comp_line + s * p.C * kD, 4u * kD * (uint32_t)p.C, bar);
+  if (p.C > 0) bulk_g2s(sm + L.comp_line, p.comp_line + s * comp_floats, 4u * comp_floats, bar);
   if (n0 > 0) {
     if (stage_k) bulk_g2s(sm + L.rec_k, p.rec_k + s * p.W * kD, rec, bar);
     bulk_g2s(sm + L.rec_u, p.rec_u + s * p.W * kD, rec, bar);
@@ -604,7 +605,8 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
           // y = A_n . k_n and A_n . q_n, formed again from the blocked k and q
           const int c = job - nrec;
           const int id = cid[c];
-          const float4* b4 = reinterpret_cast<const float4*>(cl + c * kD + 16 * qq);
+          const bool fit = p.comp_fit > 0;  // factor b_c, dense, after a_c; else the line or a unit vector
+          const float4* b4 = reinterpret_cast<const float4*>(cl + (fit ? (2 * c + 1) * kD : c * kD) + 16 * qq);
           const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
           const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
           const float4* a04 = reinterpret_cast<const float4*>(P_b + 20 * qq);
@@ -624,7 +626,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              if (id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
+              if (!fit && id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
               pa = __fmaf_rn(bs[e], __fmul_rn(av[e], kxs[e]), pa);
               pb = __fmaf_rn(bs[e], __fmul_rn(av[e], qxs[e]), pb);
             }
@@ -722,7 +724,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     for (int c = 0; c < kMaxC; ++c) {
       if (c < p.C) {
         const int id = cid[c];
-        const float a = id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f);
+        const float a = p.comp_fit > 0 ? cl[2 * c * kD + i] : (id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f));
         acc = __fmaf_rn(a, ec[c], acc);
         oo = __fmaf_rn(a, eq[c], oo);
       }
@@ -793,15 +795,17 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
     *reinterpret_cast<float4*>(kd_b + m1 * kBV + bv(j4)) =
         make_float4(__fmul_rn(pm.x, kv.x), __fmul_rn(pm.y, kv.y), __fmul_rn(pm.z, kv.z), __fmul_rn(pm.w, kv.w));
   }
-  // bd_c = P_0 . line for the row compensators (a column compensator's b_c is
-  // a unit vector; its term is applied from the line and P_0 directly).
+  // bd_c = P_0 . b_c for the row compensators (a column compensator's b_c is
+  // a unit vector; its term is applied from the line and P_0 directly) and for
+  // every fitted factor.
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
   float* bd_b = at<float>(sm, L.bd_b);
+  const bool fit = p.comp_fit > 0;
   if (tid < p.C * (kD / 4)) {
     const int c = tid >> 5, j4 = (tid & 31) << 2;
-    if (cid[c] < kD) {
-      const float4 lv = *reinterpret_cast<const float4*>(cl + c * kD + j4);
+    if (fit || cid[c] < kD) {
+      const float4 lv = *reinterpret_cast<const float4*>(cl + (fit ? (2 * c + 1) * kD : c * kD) + j4);
       float4 p0;
       if (KDA) {
         p0 = *reinterpret_cast<const float4*>(P_b + bv(j4));
@@ -821,7 +825,7 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
 // F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
 // lambda_j) P_0[j], then the compensators in order, then the records in order,
 // each an fma. Adjacent columns (2k, 2k+1) of a row travel as one packed pair.
-template <bool KDA, bool B4>
+template <bool KDA, bool B4, bool FIT>
 __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -866,7 +870,22 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
   const f32x2 one2 = f2_pack(1.0f, 1.0f);
-  for (int c = 0; c < p.C; ++c) {
+  // Fitted factors are dense: every entry takes fma(a_c[i], (P_0 . b_c)[j], S_ij).
+  for (int c = 0; c < (FIT ? p.C : 0); ++c) {
+    const ulonglong2* b4 = reinterpret_cast<const ulonglong2*>(bd_b + c * kBV + 20 * qq);
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const float a = cl[2 * c * kD + 32 * pp + 4 * w + r];
+      const f32x2 a2c = f2_pack(a, a);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const ulonglong2 b = b4[c4];
+        a2[pp][2 * c4] = f2_fma(a2c, b.x, a2[pp][2 * c4]);
+        a2[pp][2 * c4 + 1] = f2_fma(a2c, b.y, a2[pp][2 * c4 + 1]);
+      }
+    }
+  }
+  for (int c = 0; c < (FIT ? 0 : p.C); ++c) {
     const int id = cid[c];
     if (id < kD) {
       if (((id & 31) >> 2) == w) {  // warp-uniform: row id is one of this warp's rows
@@ -1016,12 +1035,172 @@ __device__ __forceinline__ void column_quads(const float* S, float* colpart) {
   *reinterpret_cast<float4*>(colpart + b * kD + 4 * cq) = make_float4(a0, a1, a2, a3);
 }
 
+// F2, fitted-factor reading of the compensators (LeapQuant §3.3: dominant
+// state components as rank-one terms; App. B.3: the state is reconstructed
+// before fitting new factors; research note 4: one compensator at a time, the
+// fit starting from the longest row). For each compensator, on the residual in
+// the tile: b = the longest row (squared length, ties to the smallest index);
+// comp_fit sweeps of {normalize b; a = R b; b = R^T a}; normalize b; a = R b;
+// store (a, b); deflate R_ij = fma(-a_i, b_j, R_ij). Normalizing multiplies by
+// one reciprocal of sqrt(b . b) (a zero b stays zero). Row products a = R b run
+// as lane-group chains over 16-column blocks and the canonical tree; column
+// products as 16-row block chains and the tree over the blocks.
+__device__ __forceinline__ float fit_inv_norm(const float* b) {
+  // every warp computes it: lane group blocks (lane & 7), the canonical tree
+  const int blk = threadIdx.x & 7;
+  float acc = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const float x = b[16 * blk + t];
+    acc = __fmaf_rn(x, x, acc);
+  }
+  const float nrm = __fsqrt_rn(tree8(acc));
+  return nrm > 0.0f ? __fdiv_rn(1.0f, nrm) : 1.0f;
+}
+
+// a = R (inv b) over the tile: thread (w, r, qq) takes rows 32pp + 4w + r,
+// columns 16qq..16qq+15 (roff from row_offsets(4w + r, qq)).
+__device__ __forceinline__ void fit_row_walk(const float* S, const float* b, float inv, float* a,
+                                             const int roff[4]) {
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float bq[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) bq[t] = __fmul_rn(b[16 * qq + t], inv);
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
+    float acc = 0.0f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
+      acc = __fmaf_rn(x.x, bq[4 * c4 + 0], acc);
+      acc = __fmaf_rn(x.y, bq[4 * c4 + 1], acc);
+      acc = __fmaf_rn(x.z, bq[4 * c4 + 2], acc);
+      acc = __fmaf_rn(x.w, bq[4 * c4 + 3], acc);
+    }
+    acc = tree8(acc);
+    if (qq == 0) a[i] = acc;
+  }
+}
+
+__device__ __forceinline__ void fit_factors_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float* av = tl.score2;       // a [128]
+  float* bvec = tl.score2 + kD;  // b [128]
+  int roff[4];
+  row_offsets(4 * w + r, qq, roff);  // rows 32pp + 4w + r share i & 7
+  const int cb = tid >> 5, cq = tid & 31;  // column walks: rows 16cb.., columns 4cq..4cq+3
+  int coff[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) coff[k] = (cq ^ ((((cq >> 3) + k) & 3) | (k & 4))) << 2;
+  __shared__ int s_best;
+  for (int c = 0; c < p.C; ++c) {
+    // the longest row of the residual
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
+      float acc = 0.0f;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
+        acc = __fmaf_rn(x.x, x.x, acc);
+        acc = __fmaf_rn(x.y, x.y, acc);
+        acc = __fmaf_rn(x.z, x.z, acc);
+        acc = __fmaf_rn(x.w, x.w, acc);
+      }
+      acc = tree8(acc);
+      if (qq == 0) tl.score[i] = acc;
+    }
+    __syncthreads();
+    if (w == 0) {
+      const int L = tid & 31;
+      float bsc = tl.score[L];
+      int bi = L;
+#pragma unroll
+      for (int e = 1; e < 4; ++e) {
+        const float v = tl.score[L + 32 * e];
+        if (v > bsc) {
+          bsc = v;
+          bi = L + 32 * e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bsc || (ov == bsc && oi < bi)) {
+          bsc = ov;
+          bi = oi;
+        }
+      }
+      if (L == 0) s_best = bi;
+    }
+    __syncthreads();
+    const int best = s_best;
+    if (tid < kD) bvec[tid] = S[sidx(best, tid)];
+    __syncthreads();
+    for (int sw = 0; sw < p.comp_fit; ++sw) {
+      fit_row_walk(S, bvec, fit_inv_norm(bvec), av, roff);
+      __syncthreads();
+      float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+      const float* base = S + 16 * cb * kD;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float ai = av[16 * cb + t];
+        const float4 x = *reinterpret_cast<const float4*>(base + t * kD + coff[t & 7]);
+        c0 = __fmaf_rn(x.x, ai, c0);
+        c1 = __fmaf_rn(x.y, ai, c1);
+        c2 = __fmaf_rn(x.z, ai, c2);
+        c3 = __fmaf_rn(x.w, ai, c3);
+      }
+      *reinterpret_cast<float4*>(tl.colpart + cb * kD + 4 * cq) = make_float4(c0, c1, c2, c3);
+      __syncthreads();
+      if (tid < kD) bvec[tid] = tree8_mem(tl.colpart + tid, kD);
+      __syncthreads();
+    }
+    const float inv = fit_inv_norm(bvec);
+    fit_row_walk(S, bvec, inv, av, roff);
+    __syncthreads();
+    float* out = p.comp_line + (s * p.C + c) * (2 * kD);
+    if (tid < kD) {
+      out[tid] = av[tid];
+      out[kD + tid] = __fmul_rn(bvec[tid], inv);
+    }
+    if (tid == 0) p.comp_id[s * p.comp_id_stride + c] = best;
+    // deflate: R_ij = fma(-a_i, b_j, R_ij)
+    float bq[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) bq[t] = __fmul_rn(bvec[16 * qq + t], inv);
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
+      const float na = -av[i];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float4* e = reinterpret_cast<float4*>(&S[i * kD + roff[c4]]);
+        float4 x = *e;
+        x.x = __fmaf_rn(na, bq[4 * c4 + 0], x.x);
+        x.y = __fmaf_rn(na, bq[4 * c4 + 1], x.y);
+        x.z = __fmaf_rn(na, bq[4 * c4 + 2], x.z);
+        x.w = __fmaf_rn(na, bq[4 * c4 + 3], x.w);
+        *e = x;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
-template <bool B4>
+template <bool B4, bool FIT>
 __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 
+  if (FIT) {
+    fit_factors_tile(p, s, S, tl);
+  } else {
   int coff[8];
   column_offsets(tid & (kD - 1), coff);
   // Column scores: thread (b = tid / 32, quad cq = tid % 32) runs the four
@@ -1131,6 +1310,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
       }
     }
     __syncthreads();
+  }
   }
 
   // F3: smoothing scales from the residual's column sums of |R|.
@@ -1328,7 +1508,7 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
 }
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
-template <bool KDA, bool B4>
+template <bool KDA, bool B4, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1352,16 +1532,16 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4>(p, s, S, tl);
+  boundary_from_tile<B4, FIT>(p, s, S, tl);
 }
 
 // Fold with the records held (any count 0..W): lq_fold.
-template <bool KDA, bool B4>
+template <bool KDA, bool B4, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1375,16 +1555,16 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4>(p, s, S, tl);
+  boundary_from_tile<B4, FIT>(p, s, S, tl);
 }
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
-template <bool KDA, bool B4>
+template <bool KDA, bool B4, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1400,7 +1580,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
@@ -1412,7 +1592,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
 }
 
 // Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
-template <bool B4>
+template <bool B4, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
@@ -1440,7 +1620,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4>(p, s, S, tl);
+  boundary_from_tile<B4, FIT>(p, s, S, tl);
 }
 
 // ---------------------------------------------------------------------------
@@ -1448,7 +1628,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
 
 static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile) {
   Params q = p;
-  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits);
+  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits, p.comp_fit);
   q.r1 = tile ? region1_bytes(q.st) : q.st.end;
   return q;
 }
@@ -1466,12 +1646,16 @@ static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, 
 
 cudaError_t launch_init(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, 0, 0, false, false, true);
-  return p.bits == 4 ? launch(k_init<true>, q, smem_of(q, true), st) : launch(k_init<false>, q, smem_of(q, true), st);
+  const bool fit = p.comp_fit > 0;
+  if (p.bits == 4) return fit ? launch(k_init<true, true>, q, smem_of(q, true), st) : launch(k_init<true, false>, q, smem_of(q, true), st);
+  return fit ? launch(k_init<false, true>, q, smem_of(q, true), st) : launch(k_init<false, false>, q, smem_of(q, true), st);
 }
 
-// Kernel K<KDA, B4> for this configuration's decay form and code width.
-#define LQ_PICK2(K, q) \
-  ((q).kda ? ((q).bits == 4 ? K<true, true> : K<true, false>) : ((q).bits == 4 ? K<false, true> : K<false, false>))
+// Kernel K<KDA, B4, FIT> for this configuration's decay form, code width and compensator form.
+#define LQ_PICK_B(K, q, KDA_) \
+  ((q).bits == 4 ? ((q).comp_fit > 0 ? K<KDA_, true, true> : K<KDA_, true, false>) \
+                 : ((q).comp_fit > 0 ? K<KDA_, false, true> : K<KDA_, false, false>))
+#define LQ_PICK2(K, q) ((q).kda ? LQ_PICK_B(K, q, true) : LQ_PICK_B(K, q, false))
 
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const int slots = append_slots(p.W, p.phase);
@@ -1503,5 +1687,6 @@ cudaError_t launch_export(const Params& p, cudaStream_t st) {
 }
 
 #undef LQ_PICK2
+#undef LQ_PICK_B
 
 }  // namespace lqi

@@ -36,7 +36,7 @@ EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", 
 class Config(ctypes.Structure):
     _fields_ = [("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("n_comp", ctypes.c_int32), ("decay_per_key", ctypes.c_int32), ("smooth", ctypes.c_int32),
-                ("lambda_floor", ctypes.c_float), ("code_bits", ctypes.c_int32)]
+                ("lambda_floor", ctypes.c_float), ("code_bits", ctypes.c_int32), ("comp_fit", ctypes.c_int32)]
 
 
 class Layout(ctypes.Structure):
@@ -103,8 +103,9 @@ def _check(rc):
         raise LQError(rc, last_error())
 
 
-def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128, code_bits=8) -> Config:
-    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor, code_bits)
+def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128, code_bits=8,
+           comp_fit=0) -> Config:
+    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor, code_bits, comp_fit)
 
 
 def default_config() -> Config:
@@ -232,7 +233,8 @@ def state_views(cfg: Config, state, n_states: int) -> dict:
         "sigma": view(L.sigma, N * D, torch.float32, (N, D)),
         "lambda": view(L.lambda_, N * D, torch.float32, (N, D)),
         "comp_id": view(L.comp_id, N * L.comp_id_stride, torch.int32, (N, L.comp_id_stride))[:, :C],
-        "comp_line": view(L.comp_line, N * C * D, torch.float32, (N, C, D)),
+        "comp_line": view(L.comp_line, N * C * D * (2 if cfg.comp_fit else 1), torch.float32,
+                          (N, C, D * (2 if cfg.comp_fit else 1))),
         "rec_k": view(L.rec_k, N * W * D, torch.float32, (N, W, D)),
         "rec_u": view(L.rec_u, N * W * D, torch.float32, (N, W, D)),
         "rec_alpha": view(L.rec_alpha, N * L.alpha_stride, torch.float32, (N, L.alpha_stride)),

@@ -64,6 +64,16 @@ def test_boundary_bytes_with_4bit_codes(L):
     assert l4.sigma - l4.codes == 1000 * 8192
 
 
+def test_fitted_factor_compensators_double_the_compensator_plane(L):
+    """With comp_fit > 0 each compensator is a factor pair a (d_v) and b (d_k)."""
+    l0 = lq.layout(lq.config(), 1)
+    l1 = lq.layout(lq.config(comp_fit=8), 1)
+    assert l1.boundary_bytes_per_state - l0.boundary_bytes_per_state == 4 * 4 * 128
+    assert l0.rec_k - l0.comp_line == 4 * 4 * 128  # C = 4 lines of 128 floats (256-byte aligned already)
+    assert l1.rec_k - l1.comp_line == 4 * 4 * 256  # C = 4 pairs of 128 + 128 floats
+    assert l1.total_bytes - l0.total_bytes == 4 * 4 * 128
+
+
 @pytest.mark.parametrize("kda", [False, True])
 @pytest.mark.parametrize("n", [1, 3, 1024, 16384])
 def test_layout_planes(L, n, kda):
@@ -90,7 +100,8 @@ def test_layout_planes(L, n, kda):
     ("window", 33, lq.ERR_UNSUPPORTED), ("n_comp", 9, lq.ERR_UNSUPPORTED), ("n_comp", -1, lq.ERR_UNSUPPORTED),
     ("decay_per_key", 2, lq.ERR_INVALID_ARG), ("smooth", 3, lq.ERR_INVALID_ARG),
     ("lambda_floor", 0.0, lq.ERR_INVALID_ARG), ("lambda_floor", float("inf"), lq.ERR_INVALID_ARG),
-    ("code_bits", 6, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG), ("code_bits", 0, lq.ERR_INVALID_ARG)])
+    ("code_bits", 6, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG), ("code_bits", 0, lq.ERR_INVALID_ARG),
+    ("comp_fit", -1, lq.ERR_INVALID_ARG), ("comp_fit", 33, lq.ERR_INVALID_ARG)])
 def test_invalid_config_rejected(L, field, value, code):
     cfg = lq.default_config()
     setattr(cfg, field, value)
