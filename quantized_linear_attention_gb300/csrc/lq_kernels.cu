@@ -469,7 +469,7 @@ __device__ __forceinline__ TokenRegs load_token(const Params& p, int64_t s) {
 // KPRE: record keys are not staged; lane group g arrives with block qq of
 // record slot g in `kpre` (read before the staging wait), and slots beyond the
 // first round of lane groups are read from global memory.
-template <bool KDA, int NT, bool FOLD, bool KPRE, bool B4>
+template <bool KDA, int NT, bool FOLD, bool KPRE, bool B4, bool FIT>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                float alpha_scalar, float beta, const TokenRegs& tk,
                                                const float4 (&kpre)[4]) {
@@ -605,7 +605,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
           // y = A_n . k_n and A_n . q_n, formed again from the blocked k and q
           const int c = job - nrec;
           const int id = cid[c];
-          const bool fit = p.comp_fit > 0;  // factor b_c, dense, after a_c; else the line or a unit vector
+          const bool fit = FIT;  // factor b_c, dense, after a_c; else the line or a unit vector
           const float4* b4 = reinterpret_cast<const float4*>(cl + (fit ? (2 * c + 1) * kD : c * kD) + 16 * qq);
           const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
           const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
@@ -724,7 +724,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     for (int c = 0; c < kMaxC; ++c) {
       if (c < p.C) {
         const int id = cid[c];
-        const float a = p.comp_fit > 0 ? cl[2 * c * kD + i] : (id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f));
+        const float a = FIT ? cl[2 * c * kD + i] : (id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f));
         acc = __fmaf_rn(a, ec[c], acc);
         oo = __fmaf_rn(a, eq[c], oo);
       }
@@ -1480,7 +1480,7 @@ __host__ __device__ inline int append_slots(int W, int phase) { return (phase >=
 
 // KPRE (the phase is stated): the record keys are not staged; each lane group
 // reads its record's key block into registers before the staging wait.
-template <bool KDA, bool KPRE, bool B4>
+template <bool KDA, bool KPRE, bool B4, bool FIT>
 __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1503,7 +1503,7 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, !KPRE, slots);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false, KPRE, B4>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 128, false, KPRE, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   if (threadIdx.x == 0) p.counts[s] = n0 + 1;
 }
 
@@ -1524,11 +1524,11 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   if (n0 < 0) return;
   const int n = n0 + 1;
   if (n < p.W) {
-    append_compute<KDA, 256, false, false, B4>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+    append_compute<KDA, 256, false, false, B4, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  append_compute<KDA, 256, true, false, B4>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 256, true, false, B4, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
@@ -1657,18 +1657,27 @@ cudaError_t launch_init(const Params& p, cudaStream_t st) {
                  : ((q).comp_fit > 0 ? K<KDA_, false, true> : K<KDA_, false, false>))
 #define LQ_PICK2(K, q) ((q).kda ? LQ_PICK_B(K, q, true) : LQ_PICK_B(K, q, false))
 
+template <bool KPRE>
+static cudaError_t launch_append_kp(const Params& q, int smem, cudaStream_t st) {
+  const bool b4 = q.bits == 4, fit = q.comp_fit > 0;
+  if (q.kda) {
+    if (b4) return fit ? launch(k_append<true, KPRE, true, true>, q, smem, st, 128)
+                       : launch(k_append<true, KPRE, true, false>, q, smem, st, 128);
+    return fit ? launch(k_append<true, KPRE, false, true>, q, smem, st, 128)
+               : launch(k_append<true, KPRE, false, false>, q, smem, st, 128);
+  }
+  if (b4) return fit ? launch(k_append<false, KPRE, true, true>, q, smem, st, 128)
+                     : launch(k_append<false, KPRE, true, false>, q, smem, st, 128);
+  return fit ? launch(k_append<false, KPRE, false, true>, q, smem, st, 128)
+             : launch(k_append<false, KPRE, false, false>, q, smem, st, 128);
+}
+
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const int slots = append_slots(p.W, p.phase);
   const bool stated = p.phase >= 0 && p.phase < p.W;
   const Params q = with_layout(p, slots, stated ? 0 : slots, true, false, false);
   const int smem = smem_of(q, false);
-  const bool b4 = p.bits == 4;
-  if (stated) {
-    if (p.kda) return b4 ? launch(k_append<true, true, true>, q, smem, st, 128) : launch(k_append<true, true, false>, q, smem, st, 128);
-    return b4 ? launch(k_append<false, true, true>, q, smem, st, 128) : launch(k_append<false, true, false>, q, smem, st, 128);
-  }
-  if (p.kda) return b4 ? launch(k_append<true, false, true>, q, smem, st, 128) : launch(k_append<true, false, false>, q, smem, st, 128);
-  return b4 ? launch(k_append<false, false, true>, q, smem, st, 128) : launch(k_append<false, false, false>, q, smem, st, 128);
+  return stated ? launch_append_kp<true>(q, smem, st) : launch_append_kp<false>(q, smem, st);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
