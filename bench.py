@@ -303,6 +303,51 @@ def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0):
     return total_ms, app, fold, clocks
 
 
+def time_staggered(wl, device, steps=50, warmup=3):
+    """Head-states at W different window phases: group g (states g*N/W ..) is re-admitted
+    by lq_state_init_range before token g, then every token is one lq_decode_step with
+    LQ_PHASE_ANY (append, then fold the windows it filled). Returns per-token ms."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+
+    W, N = wl.W, wl.n_states
+    G = N // W
+    cfg, state = setup_state(wl, device)
+    pool = Pool(wl, 4 * W, device)
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+
+    def launch(t):
+        q, k, v, a, b = pool.token(t)
+        lq.decode_step(cfg, state, N, q, k, v, a, b, o, phase=lq.PHASE_ANY)
+
+    for t in range(W):
+        if t > 0:  # a new request in these slots: its state starts from zero
+            lq.state_init_range(cfg, state, N, t * G, G if t < W - 1 else N - t * G, None)
+        launch(t)
+    tok = W
+    for _ in range(warmup * W):
+        launch(tok)
+        tok += 1
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * W + 1)]
+    ev[0].record()
+    for i in range(steps * W):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    status, bad = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
+    counts = lq.state_views(cfg, state, N)["counts"]
+    phases = torch.bincount(counts.long(), minlength=W).tolist()
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * W)]
+    del state, pool
+    torch.cuda.empty_cache()
+    return ev[0].elapsed_time(ev[-1]), d, phases
+
+
 def time_graphed(wl, steps, device):
     """Small batches are launch-bound: capture the W-1 appends and the fold step as
     two CUDA graphs per pool window and time their replays."""
@@ -528,6 +573,20 @@ def run_ours(args):
             "fold_step_us": round(fold_ms * 1e3, 2), "window_gbs": round(win_gbs, 1),
             "window_frac": round(win_gbs / hbm, 4)}
         result["batches"] = sweep
+    if rank == 0 and not args.no_stagger:
+        s_total, s_d, phases = time_staggered(wl, device)
+        s_sorted = sorted(s_d)
+        result["staggered"] = {
+            "note": f"{W} groups of {N // W} head-states, group g re-admitted from a zero state before token g "
+                    "(lq_state_init_range), then "
+                    "lq_decode_step with LQ_PHASE_ANY: each token appends every head-state, lists the windows it "
+                    f"fills and folds them (1/{W} of the head-states); 50 timed windows, 2 launches per token",
+            "head_tokens_per_s": round(N * len(s_d) / (s_total / 1e3), 1),
+            "step_us_mean": round(1e3 * s_total / len(s_d), 2), "step_us_max": round(1e3 * s_sorted[-1], 2),
+            "step_us_p50": round(1e3 * s_sorted[len(s_d) // 2], 2),
+            "in_phase_step_us_max": round(1e3 * max(fold), 2),
+            "in_phase_step_us_mean": round(1e3 * t_ms / K / W, 2),
+            "head_states_per_phase_after": phases}
     if rank == 0 and not args.no_bits4:
         b_total, b_app, b_fold, _ = time_main(wl, args, device, 1, 0, bits=4, steps=100)
         b_app_ms, b_fold_ms, b_win_ms = statistics.mean(b_app), statistics.mean(b_fold), b_total / 100
@@ -641,6 +700,7 @@ def main(argv=None):
     ap.add_argument("--no-fp32", action="store_true", help="skip the fp32-state baseline kernel")
     ap.add_argument("--no-bits4", action="store_true", help="skip the 4-bit-code run of the same workload")
     ap.add_argument("--no-fit", action="store_true", help="skip the fitted-factor compensator run")
+    ap.add_argument("--no-stagger", action="store_true", help="skip the mixed-window-phase run")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

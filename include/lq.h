@@ -95,8 +95,11 @@ typedef struct {
  *   rec_k    fp32    [s][W][d_k]               record keys, slot m-1 holds record m
  *   rec_u    fp32    [s][W][d_v]               record corrections u_m
  *   rec_alpha fp32   [s][alpha_stride]         GDN: W scalars; KDA: [W][d_k]
+ *   full_list int32  [n_states]                work list of a mixed-phase decode step:
+ *                                              the head-states whose window it filled
+ *                                              (empty between calls)
  * A 256-byte header at offset 0 carries a magic number, a hash of the config
- * and n_states, and the device status word.
+ * and n_states, the device status word and the length of the work list.
  * The boundary (codes, sigma, lambda, comp_id, comp_line) takes
  * (16384 + 512 + 512 + 4C + 512C) bytes per head-state with 8-bit codes: 1.19
  * bytes per element at C = 4, the figure of the LeapQuant summary, §4.3
@@ -104,7 +107,7 @@ typedef struct {
  */
 typedef struct {
   size_t total_bytes;
-  size_t header, counts, codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha;
+  size_t header, counts, codes, sigma, lambda, comp_id, comp_line, rec_k, rec_u, rec_alpha, full_list;
   int64_t comp_id_stride; /* int32 elements per head-state (C rounded up to a multiple of 4, at least 4) */
   int64_t alpha_stride;   /* fp32 elements per head-state in rec_alpha                               */
   int64_t boundary_bytes_per_state; /* codes + sigma + lambda + 4C id bytes + comp lines                  */
@@ -128,6 +131,20 @@ int lq_layout(const lq_config* cfg, int64_t n_states, lq_layout_t* out);
 int lq_state_init(const lq_config* cfg, void* state, int64_t n_states, const float* S0, lq_stream_t stream);
 
 /*
+ * Re-initialise head-states first .. first+count-1 of a buffer that
+ * lq_state_init set up for n_states: init-fold S0 (fp32 [count][d_v][d_k], or
+ * NULL for zero) into their boundaries and set their record counts to 0. The
+ * other head-states, the header and the status word are untouched, so a
+ * serving loop can admit a request into its slots while the rest keep their
+ * windows; requests admitted at different tokens then sit at different window
+ * phases. A buffer whose header does not match (cfg, n_states) is left
+ * unchanged and gets LQ_ERR_STATE. Errors: LQ_ERR_INVALID_ARG when
+ * first < 0, count < 0 or first + count > n_states.
+ */
+int lq_state_init_range(const lq_config* cfg, void* state, int64_t n_states, int64_t first, int64_t count,
+                        const float* S0, lq_stream_t stream);
+
+/*
  * Append one token to every head-state: read from the fixed boundary plus the
  * buffered records, u = beta (v - S_{n-1}(alpha . k)), store record n,
  * o = S_n q. No fold: a head-state that already holds W records is left
@@ -143,13 +160,19 @@ int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* 
 int lq_fold(const lq_config* cfg, void* state, int64_t n_states, lq_stream_t stream);
 
 /*
- * One decode token for every head-state: append, and when that fills the
- * window (count == W), fold in the same kernel while the state is on chip.
+ * One decode token for every head-state: append, and fold every head-state
+ * whose window that fills (count == W).
  * `phase` is the record count every head-state holds before this call
- * (0..W-1), which lets the library launch the append-only kernel for the W-1
- * steps that cannot fold; a head-state whose count differs is left unchanged
- * and sets LQ_ERR_PHASE. LQ_PHASE_ANY accepts any count (each head-state
- * folds when its own window fills). Arguments otherwise as lq_append.
+ * (0..W-1). It lets the library launch the append-only kernel for the W-1
+ * steps that cannot fold, and fuse the fold into the append kernel at phase
+ * W-1 while the state is on chip; a head-state whose count differs is left
+ * unchanged and sets LQ_ERR_PHASE.
+ * LQ_PHASE_ANY accepts any count 0..W-1 (head-states at different window
+ * phases, e.g. requests admitted at different tokens): the append kernel puts
+ * the head-states whose window it fills on the buffer's work list, and a
+ * second kernel folds them, spread over every SM. With phases spread evenly,
+ * 1/W of the head-states fold per token and no token carries a whole fold.
+ * Arguments otherwise as lq_append.
  */
 int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
                    const float* k, const float* v, const float* alpha, const float* beta, float* o,

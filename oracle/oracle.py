@@ -158,6 +158,19 @@ class OracleState:
             if rc != 0:
                 raise RuntimeError(f"orc_init_state failed: {rc}")
 
+    def init_range(self, first, count, S0=None, diags=None):
+        """Init-fold states first .. first+count-1 from S0 [count][dv][dk] (None: zero);
+        the other states keep their boundaries and records."""
+        L = lib()
+        if S0 is not None:
+            S0 = _f32(S0).reshape(count, self.dv, self.dk)
+        for i in range(count):
+            p = None if S0 is None else S0[i].ctypes.data
+            d = None if diags is None else ctypes.byref(diags[i].c)
+            rc = L.orc_init_state(ctypes.byref(self.cfg), ctypes.byref(self.batch), first + i, p, d)
+            if rc != 0:
+                raise RuntimeError(f"orc_init_state failed: {rc}")
+
     def append(self, q, k, v, alpha, beta):
         """Append one token to every state; returns o [N][dv] (float64)."""
         return self.run(np.asarray(q)[None], np.asarray(k)[None], np.asarray(v)[None], np.asarray(alpha)[None],

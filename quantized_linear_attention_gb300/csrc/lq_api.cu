@@ -98,6 +98,8 @@ void make_layout(const lq_config* c, int64_t n, lq_layout_t* L) {
   off = align256(off + sizeof(Header));
   L->counts = off;
   off = align256(off + 4 * N);
+  L->full_list = off;
+  off = align256(off + 4 * N);
   L->codes = off;
   off = align256(off + N * D * D * (size_t)c->code_bits / 8);
   L->sigma = off;
@@ -181,6 +183,7 @@ Params make_params(const lq_config* c, void* state, int64_t n) {
   p.alpha_stride = L.alpha_stride;
   p.hdr = reinterpret_cast<Header*>(base + L.header);
   p.counts = reinterpret_cast<int32_t*>(base + L.counts);
+  p.full_list = reinterpret_cast<int32_t*>(base + L.full_list);
   p.codes = reinterpret_cast<int8_t*>(base + L.codes);
   p.sigma = reinterpret_cast<float*>(base + L.sigma);
   p.lambda = reinterpret_cast<float*>(base + L.lambda);
@@ -269,6 +272,24 @@ int lq_state_init(const lq_config* cfg, void* state, int64_t n_states, const flo
   return launched(lqi::launch_init(p, (cudaStream_t)stream), "lq_state_init launch");
 }
 
+int lq_state_init_range(const lq_config* cfg, void* state, int64_t n_states, int64_t first, int64_t count,
+                        const float* S0, lq_stream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if ((rc = check_n(n_states))) return rc;
+  if (first < 0 || count < 0 || first > n_states || count > n_states - first)
+    return fail(LQ_ERR_INVALID_ARG, "range [%lld, %lld + %lld) is not inside 0..%lld", (long long)first,
+                (long long)first, (long long)count, (long long)n_states);
+  if (count == 0) return ok();
+  int dev = 0;
+  if ((rc = check_common(cfg, state, n_states, stream, &dev))) return rc;
+  if (S0 && (rc = check_ptr(S0, "S0", 16, dev))) return rc;
+  Params p = make_params(cfg, state, n_states);
+  p.S0 = S0;
+  p.first = first;
+  return launched(lqi::launch_init_range(p, count, (cudaStream_t)stream), "lq_state_init_range launch");
+}
+
 int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k, const float* v,
               const float* alpha, const float* beta, float* o, lq_stream_t stream) {
   int dev = 0;
@@ -312,8 +333,16 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
   p.o = o;
   p.phase = phase;
   // A stated phase below W-1 cannot fill the window: the append-only kernel
-  // needs no fold workspace and runs at higher occupancy.
-  if (phase != LQ_PHASE_ANY && phase < cfg->window - 1)
+  // needs no fold workspace and runs at higher occupancy. At W-1 every
+  // head-state folds, in the append kernel. Mixed phases: append (listing the
+  // windows filled), then fold the list.
+  if (phase == LQ_PHASE_ANY) {
+    p.push_full = 1;
+    cudaError_t e = lqi::launch_append(p, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = lqi::launch_fold_listed(p, (cudaStream_t)stream);
+    return launched(e, "lq_decode_step launch");
+  }
+  if (phase < cfg->window - 1)
     return launched(lqi::launch_append(p, (cudaStream_t)stream), "lq_decode_step launch");
   return launched(lqi::launch_step(p, (cudaStream_t)stream), "lq_decode_step launch");
 }

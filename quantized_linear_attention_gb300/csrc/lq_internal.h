@@ -9,7 +9,7 @@
 namespace lqi {
 
 constexpr uint32_t kMagic = 0x4C513847u;  // "GQ8L"
-constexpr uint32_t kLayoutVersion = 1;
+constexpr uint32_t kLayoutVersion = 2;
 constexpr int kD = 128;       // d_k = d_v
 constexpr int kMaxW = 32;     // records per window
 constexpr int kMaxC = 8;      // compensators per head-state
@@ -24,7 +24,9 @@ struct Header {
   int32_t status;     // first device-side error (lq_status), 0 when clean
   int32_t reserved0;
   int64_t bad_state;  // head-state index that set `status`
-  uint8_t pad[256 - 40];
+  int32_t full_n;     // entries on the full-window list (mixed-phase decode step)
+  int32_t fold_done;  // CTAs of the list fold that have finished
+  uint8_t pad[256 - 48];
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
@@ -47,11 +49,14 @@ struct Params {
   int comp_fit;  // 0: outlier-line compensators; s > 0: factors fitted by s sweeps
   float lambda_floor;
   int phase;  // expected record count before the call, or -1
+  int push_full;  // append: list the head-states whose window this token fills
   int64_t n_states;
+  int64_t first;  // range init: first head-state of the range
   uint64_t cfg_hash;
   int64_t comp_id_stride, alpha_stride;
   Header* hdr;
   int32_t* counts;
+  int32_t* full_list;
   int8_t* codes;
   float* sigma;
   float* lambda;
@@ -89,6 +94,8 @@ cudaError_t launch_init(const Params& p, cudaStream_t st);
 cudaError_t launch_append(const Params& p, cudaStream_t st);
 cudaError_t launch_step(const Params& p, cudaStream_t st);
 cudaError_t launch_fold(const Params& p, cudaStream_t st);
+cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st);
+cudaError_t launch_fold_listed(const Params& p, cudaStream_t st);
 cudaError_t launch_export(const Params& p, cudaStream_t st);
 cudaError_t launch_fp32_step(const Fp32Params& p, cudaStream_t st);
 

@@ -1425,9 +1425,10 @@ struct StageInfo {
 };
 
 __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int known_n0, const Stage& L,
-                                                 uint64_t* bar, StageInfo* sh, bool stage_k, int max_n0) {
+                                                 uint64_t* bar, StageInfo* sh, bool stage_k, int max_n0,
+                                                 bool init_bar = true) {
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    if (init_bar) mbar_init(bar, 1);
     int n0 = known_n0;
     if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k);
     const int c = p.counts[s];
@@ -1444,18 +1445,19 @@ __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int
   return *sh;
 }
 
-// Bounded wait for the copies, then the checks. Returns the record count held
-// (>= 0) or -1 after recording an error; uniform over the CTA.
+// Bounded wait for the copies (phase `parity` of the barrier), then the
+// checks. Returns the record count held (>= 0), or after recording an error -1
+// (the copies have landed) or -2 (the wait gave up); uniform over the CTA.
 __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t* bar, const StageInfo& si,
-                                            bool append) {
+                                            bool append, uint32_t parity = 0) {
   const int n0 = si.issued, cnt = si.cnt;
   const bool hdr = si.hdr != 0;
   if (n0 >= 0) {
-    const bool ok = mbar_wait_bounded(bar, 0);
+    const bool ok = mbar_wait_bounded(bar, parity);
     if (__syncthreads_or(!ok)) {
-      if (!ok) (void)mbar_wait_bounded(bar, 0);  // one more bounded chance for copies in flight
+      if (!ok) (void)mbar_wait_bounded(bar, parity);  // one more bounded chance for copies in flight
       if (threadIdx.x == 0) set_error(p, LQ_ERR_TIMEOUT, s);
-      return -1;
+      return -2;
     }
   }
   int err = 0;
@@ -1478,9 +1480,22 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
 // lq_append. With a stated phase the staging area holds exactly `phase` records.
 __host__ __device__ inline int append_slots(int W, int phase) { return (phase >= 0 && phase < W) ? phase : W - 1; }
 
-// KPRE (the phase is stated): the record keys are not staged; each lane group
-// reads its record's key block into registers before the staging wait.
-template <bool KDA, bool KPRE, bool B4, bool FIT>
+// Lane group grp's block of record slot grp's key, when that slot is one of
+// the n0 records held.
+__device__ __forceinline__ void prefetch_key(const Params& p, int64_t s, int n0, float4 (&kpre)[4]) {
+  const int grp = threadIdx.x >> 3, qq = threadIdx.x & 7;
+  if (grp < n0) {
+    const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * p.W + grp) * kD + 16 * qq);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) kpre[c4] = src[c4];
+  }
+}
+
+// The record keys are not staged: each lane group reads its record's key block
+// into registers before the staging wait -- at once when the phase is stated,
+// else once thread 0 has read the record count. With p.push_full the
+// head-states whose window this token fills are put on the full-window list.
+template <bool KDA, bool B4, bool FIT>
 __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1492,19 +1507,22 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
   const TokenRegs tk = load_token(p, s);
   float4 kpre[4];
-  if (KPRE) {
-    const int grp = threadIdx.x >> 3, qq = threadIdx.x & 7;
-    if (grp < known) {
-      const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * p.W + grp) * kD + 16 * qq);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) kpre[c4] = src[c4];
-    }
-  }
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, !KPRE, slots);
+  if (known >= 0) prefetch_key(p, s, known, kpre);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
+  if (known < 0) prefetch_key(p, s, si.issued, kpre);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false, KPRE, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
-  if (threadIdx.x == 0) p.counts[s] = n0 + 1;
+  append_compute<KDA, 128, false, true, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  if (threadIdx.x == 0) {
+    p.counts[s] = n0 + 1;
+    if (p.push_full && n0 + 1 == p.W) {
+      const int slot = atomicAdd(&p.hdr->full_n, 1);
+      if (slot >= 0 && slot < p.n_states)
+        p.full_list[slot] = (int32_t)s;
+      else
+        set_error(p, LQ_ERR_STATE, s);
+    }
+  }
 }
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
@@ -1540,16 +1558,10 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   boundary_from_tile<B4, FIT>(p, s, S, tl);
 }
 
-// Fold with the records held (any count 0..W): lq_fold.
+// F0-F6 on a staged head-state holding n records.
 template <bool KDA, bool B4, bool FIT>
-__global__ void __launch_bounds__(256, 3) k_fold(Params p) {
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ StageInfo s_info;
-  const int64_t s = blockIdx.x;
+__device__ __forceinline__ void fold_staged(const Params& p, int64_t s, int n) {
   const Stage& L = p.st;
-  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, true, p.W);
-  const int n = stage_finish(p, s, &bar, si, false);
-  if (n < 0) return;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
                       at<float>(lq_dyn_smem, L.P_b));
   __syncthreads();
@@ -1561,6 +1573,68 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
   boundary_from_tile<B4, FIT>(p, s, S, tl);
+}
+
+// Fold with the records held (any count 0..W): lq_fold.
+template <bool KDA, bool B4, bool FIT>
+__global__ void __launch_bounds__(256, 3) k_fold(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ StageInfo s_info;
+  const int64_t s = blockIdx.x;
+  const StageInfo si = stage_start(p, s, -1, p.st, &bar, &s_info, true, p.W);
+  const int n = stage_finish(p, s, &bar, si, false);
+  if (n < 0) return;
+  fold_staged<KDA, B4, FIT>(p, s, n);
+}
+
+// Fold the head-states on the full-window list (the second kernel of a
+// mixed-phase decode step). Persistent: CTA b folds list entries b, b + G,
+// b + 2G, ... (G = gridDim.x, at most the CTAs that fit on the GPU at once),
+// so the few head-states whose window fills this token are spread over every
+// SM. Each entry must hold W records. The last CTA to finish empties the list.
+template <bool KDA, bool B4, bool FIT>
+__global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ StageInfo s_info;
+  __shared__ int s_nfull;
+  if (threadIdx.x == 0) {
+    int nf = -1;
+    if (header_ok(p)) {
+      nf = *reinterpret_cast<volatile int32_t*>(&p.hdr->full_n);
+      if (nf < 0 || nf > p.n_states) {
+        if (blockIdx.x == 0) set_error(p, LQ_ERR_STATE, -1);
+        nf = 0;
+      }
+    } else if (blockIdx.x == 0) {
+      set_error(p, LQ_ERR_STATE, -1);
+    }
+    s_nfull = nf;
+  }
+  __syncthreads();
+  const int nfull = s_nfull;
+  if (nfull < 0) return;  // not this configuration's buffer: touch nothing
+  uint32_t parity = 0;
+  for (int64_t t = blockIdx.x; t < nfull; t += gridDim.x) {
+    const int64_t s = p.full_list[t];
+    if (s < 0 || s >= p.n_states) {
+      if (threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
+      continue;
+    }
+    const StageInfo si = stage_start(p, s, p.W, p.st, &bar, &s_info, true, p.W, parity == 0 && t == blockIdx.x);
+    const int n = stage_finish(p, s, &bar, si, false, parity);
+    parity ^= 1u;
+    if (n == -2) break;  // copies may still land: the barrier is not reused
+    if (n == p.W) fold_staged<KDA, B4, FIT>(p, s, n);
+    else if (n >= 0 && threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
+    __syncthreads();  // the next entry's copies overwrite what this one read
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.hdr->fold_done, 1) == (int)gridDim.x - 1) {
+      p.hdr->full_n = 0;
+      p.hdr->fold_done = 0;
+    }
+  }
 }
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
@@ -1591,13 +1665,17 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   }
 }
 
-// Init-fold: F2-F6 on S0 (or zero). Block 0 writes the header.
+// Init-fold: F2-F6 on S0 (or zero). The whole buffer (p.first < 0): block 0
+// writes the header. A range (p.first >= 0): block b re-initialises head-state
+// first + b from S0 row block b, and the header must already match.
 template <bool B4, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_init(Params p) {
-  const int64_t s = blockIdx.x;
+  __shared__ int s_ok;
+  const bool range = p.first >= 0;
+  const int64_t s = (range ? p.first : 0) + blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
-  if (s == 0 && tid == 0) {
+  if (!range && blockIdx.x == 0 && tid == 0) {
     p.hdr->magic = kMagic;
     p.hdr->version = kLayoutVersion;
     p.hdr->cfg_hash = p.cfg_hash;
@@ -1605,13 +1683,23 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
     p.hdr->status = 0;
     p.hdr->reserved0 = 0;
     p.hdr->bad_state = -1;
+    p.hdr->full_n = 0;
+    p.hdr->fold_done = 0;
+  }
+  if (range) {
+    if (tid == 0) {
+      s_ok = header_ok(p) ? 1 : 0;
+      if (!s_ok) set_error(p, LQ_ERR_STATE, s);
+    }
+    __syncthreads();
+    if (!s_ok) return;
   }
   float acc[4][16];
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
     if (p.S0) {
-      load16(p.S0 + (s * kD + i) * kD + 16 * qq, acc[pp]);
+      load16(p.S0 + ((int64_t)blockIdx.x * kD + i) * kD + 16 * qq, acc[pp]);
     } else {
 #pragma unroll
       for (int t = 0; t < 16; ++t) acc[pp][t] = 0.0f;
@@ -1635,21 +1723,38 @@ static Params with_layout(const Params& p, int slots_u, int slots_k, bool append
 static int smem_of(const Params& q, bool tile) { return tile ? q.r1 + kTailBytes : q.st.end; }
 
 template <typename K>
-static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, int threads = 256) {
+static cudaError_t set_smem(K kernel, int smem) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+// One CTA per head-state (grid = p.n_states), or `grid` CTAs.
+template <typename K>
+static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, int threads = 256, int64_t grid = -1) {
+  const cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3((unsigned)p.n_states), dim3(threads), (size_t)smem, st>>>(p);
+  kernel<<<dim3((unsigned)(grid >= 0 ? grid : p.n_states)), dim3(threads), (size_t)smem, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_init(const Params& p, cudaStream_t st) {
+static cudaError_t init_any(const Params& p, int64_t grid, cudaStream_t st) {
   const Params q = with_layout(p, 0, 0, false, false, true);
+  const int smem = smem_of(q, true);
   const bool fit = p.comp_fit > 0;
-  if (p.bits == 4) return fit ? launch(k_init<true, true>, q, smem_of(q, true), st) : launch(k_init<true, false>, q, smem_of(q, true), st);
-  return fit ? launch(k_init<false, true>, q, smem_of(q, true), st) : launch(k_init<false, false>, q, smem_of(q, true), st);
+  if (p.bits == 4)
+    return fit ? launch(k_init<true, true>, q, smem, st, 256, grid) : launch(k_init<true, false>, q, smem, st, 256, grid);
+  return fit ? launch(k_init<false, true>, q, smem, st, 256, grid) : launch(k_init<false, false>, q, smem, st, 256, grid);
 }
+
+cudaError_t launch_init(const Params& p, cudaStream_t st) {
+  Params q = p;
+  q.first = -1;
+  return init_any(q, p.n_states, st);
+}
+
+cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st) { return init_any(p, count, st); }
 
 // Kernel K<KDA, B4, FIT> for this configuration's decay form, code width and compensator form.
 #define LQ_PICK_B(K, q, KDA_) \
@@ -1657,27 +1762,11 @@ cudaError_t launch_init(const Params& p, cudaStream_t st) {
                  : ((q).comp_fit > 0 ? K<KDA_, false, true> : K<KDA_, false, false>))
 #define LQ_PICK2(K, q) ((q).kda ? LQ_PICK_B(K, q, true) : LQ_PICK_B(K, q, false))
 
-template <bool KPRE>
-static cudaError_t launch_append_kp(const Params& q, int smem, cudaStream_t st) {
-  const bool b4 = q.bits == 4, fit = q.comp_fit > 0;
-  if (q.kda) {
-    if (b4) return fit ? launch(k_append<true, KPRE, true, true>, q, smem, st, 128)
-                       : launch(k_append<true, KPRE, true, false>, q, smem, st, 128);
-    return fit ? launch(k_append<true, KPRE, false, true>, q, smem, st, 128)
-               : launch(k_append<true, KPRE, false, false>, q, smem, st, 128);
-  }
-  if (b4) return fit ? launch(k_append<false, KPRE, true, true>, q, smem, st, 128)
-                     : launch(k_append<false, KPRE, true, false>, q, smem, st, 128);
-  return fit ? launch(k_append<false, KPRE, false, true>, q, smem, st, 128)
-             : launch(k_append<false, KPRE, false, false>, q, smem, st, 128);
-}
-
+// Staging holds `phase` records (W-1 when the phase is not stated); the keys
+// travel in registers.
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
-  const int slots = append_slots(p.W, p.phase);
-  const bool stated = p.phase >= 0 && p.phase < p.W;
-  const Params q = with_layout(p, slots, stated ? 0 : slots, true, false, false);
-  const int smem = smem_of(q, false);
-  return stated ? launch_append_kp<true>(q, smem, st) : launch_append_kp<false>(q, smem, st);
+  const Params q = with_layout(p, append_slots(p.W, p.phase), 0, true, false, false);
+  return launch(LQ_PICK2(k_append, q), q, smem_of(q, false), st, 128);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
@@ -1688,6 +1777,23 @@ cudaError_t launch_step(const Params& p, cudaStream_t st) {
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, p.W, p.W, false, true, true);
   return launch(LQ_PICK2(k_fold, q), q, smem_of(q, true), st);
+}
+
+// As many CTAs as fit on the GPU at once (never more than head-states).
+cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
+  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  const int smem = smem_of(q, true);
+  auto kernel = LQ_PICK2(k_fold_listed, q);
+  cudaError_t e = set_smem(kernel, smem);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > p.n_states) grid = p.n_states;
+  kernel<<<dim3((unsigned)grid), dim3(256), (size_t)smem, st>>>(q);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {

@@ -28,9 +28,9 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
                 -4: "LQ_ERR_CUDA", -5: "LQ_ERR_TIMEOUT", -6: "LQ_ERR_PHASE", -7: "LQ_ERR_STATE"}
 
 # Every symbol include/lq.h declares.
-EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_append", "lq_fold",
-           "lq_decode_step", "lq_export_state", "lq_fp32_decode_step", "lq_get_status", "lq_clear_status",
-           "lq_last_error", "lq_version")
+EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_state_init_range", "lq_append",
+           "lq_fold", "lq_decode_step", "lq_export_state", "lq_fp32_decode_step", "lq_get_status",
+           "lq_clear_status", "lq_last_error", "lq_version")
 
 
 class Config(ctypes.Structure):
@@ -41,7 +41,8 @@ class Config(ctypes.Structure):
 
 class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("total_bytes", "header", "counts", "codes", "sigma", "lambda_",
-                                                "comp_id", "comp_line", "rec_k", "rec_u", "rec_alpha")] + \
+                                                "comp_id", "comp_line", "rec_k", "rec_u", "rec_alpha",
+                                                "full_list")] + \
                [("comp_id_stride", ctypes.c_int64), ("alpha_stride", ctypes.c_int64),
                 ("boundary_bytes_per_state", ctypes.c_int64)]
 
@@ -76,6 +77,7 @@ def load():
         "lq_state_bytes": (ctypes.c_size_t, [cfgp, i64]),
         "lq_layout": (ctypes.c_int, [cfgp, i64, ctypes.POINTER(Layout)]),
         "lq_state_init": (ctypes.c_int, [cfgp, P, i64, P, P]),
+        "lq_state_init_range": (ctypes.c_int, [cfgp, P, i64, i64, i64, P, P]),
         "lq_append": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
         "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
@@ -169,6 +171,12 @@ def state_init(cfg, state, n_states, S0=None, stream=None):
                                 _stream(stream)))
 
 
+def state_init_range(cfg, state, n_states, first, count, S0=None, stream=None):
+    """Re-initialise head-states first .. first+count-1 from S0 [count][d_v][d_k] (None: zero)."""
+    _check(load().lq_state_init_range(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(first), int(count),
+                                      _ptr(S0, "S0", _f32()), _stream(stream)))
+
+
 def append(cfg, state, n_states, q, k, v, alpha, beta, o, stream=None):
     f = _f32()
     _check(load().lq_append(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(q, "q", f), _ptr(k, "k", f),
@@ -238,4 +246,5 @@ def state_views(cfg: Config, state, n_states: int) -> dict:
         "rec_k": view(L.rec_k, N * W * D, torch.float32, (N, W, D)),
         "rec_u": view(L.rec_u, N * W * D, torch.float32, (N, W, D)),
         "rec_alpha": view(L.rec_alpha, N * L.alpha_stride, torch.float32, (N, L.alpha_stride)),
+        "full_list": view(L.full_list, N, torch.int32, (N,)),
     }

@@ -79,20 +79,20 @@ def test_fitted_factor_compensators_double_the_compensator_plane(L):
 def test_layout_planes(L, n, kda):
     cfg = lq.config(kda=kda)
     lay = lq.layout(cfg, n)
-    offs = [lay.header, lay.counts, lay.codes, lay.sigma, lay.lambda_, lay.comp_id, lay.comp_line, lay.rec_k,
-            lay.rec_u, lay.rec_alpha, lay.total_bytes]
+    offs = [lay.header, lay.counts, lay.full_list, lay.codes, lay.sigma, lay.lambda_, lay.comp_id, lay.comp_line,
+            lay.rec_k, lay.rec_u, lay.rec_alpha, lay.total_bytes]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)
-    assert lay.codes - lay.counts >= 4 * n
+    assert lay.full_list - lay.counts >= 4 * n and lay.codes - lay.full_list >= 4 * n
     assert lay.sigma - lay.codes >= n * 128 * 128
     assert lay.comp_line - lay.comp_id >= 4 * n * lay.comp_id_stride
     assert lay.rec_u - lay.rec_k >= 4 * n * 16 * 128
     assert lay.alpha_stride == (16 * 128 if kda else 16)
     assert lq.state_bytes(cfg, n) == lay.total_bytes
     per_state = (lay.total_bytes - 256) / n
-    # GDN: 4 + 16384 + 512 + 512 + 16 + 2048 + 8192 + 8192 + 64 = 35924 B per head-state, plus padding
-    base = 35924 + (8192 - 64 if kda else 0)
-    assert base <= per_state <= base + 10 * 256 / n + 1
+    # GDN: 4 + 4 + 16384 + 512 + 512 + 16 + 2048 + 8192 + 8192 + 64 = 35928 B per head-state, plus padding
+    base = 35928 + (8192 - 64 if kda else 0)
+    assert base <= per_state <= base + 11 * 256 / n + 1
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -122,8 +122,14 @@ def test_invalid_sizes_and_nulls_rejected_on_host(L):
                  lambda: L.lq_fold(ctypes.byref(cfg), None, 0, None),
                  lambda: L.lq_append(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, None),
                  lambda: L.lq_decode_step(ctypes.byref(cfg), None, 0, -1, None, None, None, None, None, None, None),
-                 lambda: L.lq_export_state(ctypes.byref(cfg), None, 0, None, None)):
+                 lambda: L.lq_export_state(ctypes.byref(cfg), None, 0, None, None),
+                 lambda: L.lq_state_init_range(ctypes.byref(cfg), None, 0, 0, 0, None, None),
+                 lambda: L.lq_state_init_range(ctypes.byref(cfg), None, 8, 8, 0, None, None)):
         assert call() == lq.OK
+    # a range outside 0..n_states is rejected before the device is looked at
+    for first, count in ((-1, 1), (0, -1), (7, 2), (9, 0), (1, 2**40)):
+        assert L.lq_state_init_range(ctypes.byref(cfg), None, 8, first, count, None, None) == lq.ERR_INVALID_ARG
+        assert "range" in lq.last_error()
     # a bad phase is rejected before anything else is looked at
     assert L.lq_decode_step(ctypes.byref(cfg), None, 0, 16, None, None, None, None, None, None, None) == \
         lq.ERR_INVALID_ARG
