@@ -348,6 +348,48 @@ def time_staggered(wl, device, steps=50, warmup=3):
     return ev[0].elapsed_time(ev[-1]), d, phases
 
 
+def time_two_record(wl, device, steps=50, warmup=3):
+    """Two-record tokens (DeltaProduct with two steps): W/2 lq_decode_step2 calls per
+    window at stated phases 0, 2, ..., W-2; the last one also folds (second kernel).
+    Sub-step 1 takes generator token 2t, sub-step 2 and the query token 2t+1."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+
+    W, N = wl.W, wl.n_states
+    per_win = W // 2
+    cfg, state = setup_state(wl, device)
+    pool = Pool(wl, 4 * W, device)
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+
+    def launch(t):
+        q, k2, v2, _, b2 = pool.token(2 * t + 1)
+        _, k1, v1, a, b1 = pool.token(2 * t)
+        lq.decode_step2(cfg, state, N, q, k1, v1, b1, k2, v2, b2, a, o, phase=(2 * t) % W)
+
+    tok = 0
+    for _ in range(warmup * per_win):
+        launch(tok)
+        tok += 1
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * per_win + 1)]
+    ev[0].record()
+    for i in range(steps * per_win):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    status, bad = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * per_win)]
+    app = [d[i] for i in range(len(d)) if i % per_win != per_win - 1]
+    fold = [d[i] for i in range(len(d)) if i % per_win == per_win - 1]
+    del state, pool
+    torch.cuda.empty_cache()
+    return ev[0].elapsed_time(ev[-1]), app, fold
+
+
 def time_graphed(wl, steps, device):
     """Small batches are launch-bound: capture the W-1 appends and the fold step as
     two CUDA graphs per pool window and time their replays."""
@@ -587,6 +629,18 @@ def run_ours(args):
             "in_phase_step_us_max": round(1e3 * max(fold), 2),
             "in_phase_step_us_mean": round(1e3 * t_ms / K / W, 2),
             "head_states_per_phase_after": phases}
+    if rank == 0 and not args.no_two:
+        t_total, t_app, t_fold = time_two_record(wl, device)
+        n_tok = len(t_app) + len(t_fold)
+        result["two_record"] = {
+            "note": f"two-record tokens (DeltaProduct with two steps, lq_decode_step2): {W // 2} tokens per "
+                    f"{W}-record window, one kernel per token reads the boundary once; the last token of a window "
+                    "adds the list fold; 50 timed windows",
+            "head_tokens_per_s": round(N * n_tok / (t_total / 1e3), 1),
+            "token_us_mean": round(1e3 * t_total / n_tok, 2),
+            "append2_us": round(1e3 * statistics.mean(t_app), 2),
+            "fold_token_us": round(1e3 * statistics.mean(t_fold), 2),
+            "two_one_record_steps_us": round(2e3 * t_ms / K / W, 2)}
     if rank == 0 and not args.no_bits4:
         b_total, b_app, b_fold, _ = time_main(wl, args, device, 1, 0, bits=4, steps=100)
         b_app_ms, b_fold_ms, b_win_ms = statistics.mean(b_app), statistics.mean(b_fold), b_total / 100
@@ -701,6 +755,7 @@ def main(argv=None):
     ap.add_argument("--no-bits4", action="store_true", help="skip the 4-bit-code run of the same workload")
     ap.add_argument("--no-fit", action="store_true", help="skip the fitted-factor compensator run")
     ap.add_argument("--no-stagger", action="store_true", help="skip the mixed-window-phase run")
+    ap.add_argument("--no-two", action="store_true", help="skip the two-record-token run")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

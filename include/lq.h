@@ -179,6 +179,29 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
                    lq_stream_t stream);
 
 /*
+ * One two-record token for every head-state: a token whose update is two
+ * rank-one sub-steps, as LeapQuant App. A ("Instances of the general update")
+ * represents a DeltaProduct token with two steps:
+ *   u1 = beta1 (v1 - S_{n-1}(alpha . k1)),  S_n     = S_{n-1} Diag(alpha) + u1 k1^T,
+ *   u2 = beta2 (v2 - S_n k2),               S_{n+1} = S_n + u2 k2^T,
+ *   o  = S_{n+1} q.
+ * It stores records n = (k1, u1, alpha) and n+1 = (k2, u2, 1): exactly what
+ * lq_decode_step does for (k1, v1, beta1, alpha) and then for (k2, v2, beta2,
+ * alpha = 1), but with one read of the boundary. When the second record fills
+ * the window (count == W), the head-state is folded in the same call.
+ * `phase` is the record count every head-state holds before the call (0..W-2),
+ * or LQ_PHASE_ANY. A head-state without room for both records (count > W-2)
+ * is left unchanged and sets LQ_ERR_WINDOW_FULL; with an even W and only
+ * two-record tokens that cannot happen.
+ *   q, k1, k2 fp32 [n_states][d_k];  v1, v2, o fp32 [n_states][d_v]
+ *   alpha fp32 [n_states] (GDN) or [n_states][d_k] (KDA);  beta1, beta2 fp32 [n_states]
+ * Errors: as lq_decode_step; LQ_ERR_UNSUPPORTED when W < 2.
+ */
+int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
+                    const float* k1, const float* v1, const float* beta1, const float* k2, const float* v2,
+                    const float* beta2, const float* alpha, float* o, lq_stream_t stream);
+
+/*
  * Write the state each head-state stands for, S_n = boundary x Diag(A_n) plus
  * the buffered records, in original coordinates (the fold's reconstruction,
  * without rounding), to S_out fp32 [n_states][d_v][d_k]. The state is unchanged.

@@ -347,6 +347,42 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
   return launched(lqi::launch_step(p, (cudaStream_t)stream), "lq_decode_step launch");
 }
 
+int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
+                    const float* k1, const float* v1, const float* beta1, const float* k2, const float* v2,
+                    const float* beta2, const float* alpha, float* o, lq_stream_t stream) {
+  int dev = 0;
+  int rc = check_common(cfg, state, n_states, stream, &dev);
+  if (rc) return rc;
+  if (cfg->window < 2) return fail(LQ_ERR_UNSUPPORTED, "two-record tokens need a window of at least 2 records");
+  if (phase != LQ_PHASE_ANY && (phase < 0 || phase > cfg->window - 2))
+    return fail(LQ_ERR_INVALID_ARG, "phase must be LQ_PHASE_ANY or 0..W-2 (got %d)", phase);
+  if (n_states == 0) return ok();
+  if ((rc = check_tokens(cfg, n_states, dev, q, k1, v1, alpha, beta1, o))) return rc;
+  if ((rc = check_ptr(k2, "k2", 16, dev)) || (rc = check_ptr(v2, "v2", 16, dev)) ||
+      (rc = check_ptr(beta2, "beta2", 4, dev)))
+    return rc;
+  const size_t vec = (size_t)n_states * kD * sizeof(float);
+  if (overlaps(o, vec, k2, vec) || overlaps(o, vec, v2, vec) || overlaps(o, vec, beta2, (size_t)n_states * 4))
+    return fail(LQ_ERR_INVALID_ARG, "o overlaps an input");
+  Params p = make_params(cfg, state, n_states);
+  p.q = q;
+  p.k = k1;
+  p.v = v1;
+  p.beta = beta1;
+  p.k2 = k2;
+  p.v2 = v2;
+  p.beta2 = beta2;
+  p.alpha = alpha;
+  p.o = o;
+  p.phase = phase;
+  // The window can fill only at phase W-2 (or at any phase when not stated):
+  // then the filled head-states are listed and folded by a second kernel.
+  p.push_full = (phase == LQ_PHASE_ANY || phase == cfg->window - 2) ? 1 : 0;
+  cudaError_t e = lqi::launch_append2(p, (cudaStream_t)stream);
+  if (e == cudaSuccess && p.push_full) e = lqi::launch_fold_listed(p, (cudaStream_t)stream);
+  return launched(e, "lq_decode_step2 launch");
+}
+
 int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, float* S_out, lq_stream_t stream) {
   int dev = 0;
   int rc = check_common(cfg, state, n_states, stream, &dev);

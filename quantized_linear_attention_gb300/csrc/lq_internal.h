@@ -39,6 +39,8 @@ struct Stage {
   int kn_b, qn_b, zk_b, zq_b, lam_b, kd_b, bd_b, P_b;
   // computed, dense
   int basek, baseq, P, g, h, ec, eq;
+  // two-record tokens: the second record's key, read vector and sums
+  int k2n_b, zk2_b, basek2, g2, ec2;
   int end;
 };
 
@@ -70,6 +72,9 @@ struct Params {
   const float* v;
   const float* alpha;
   const float* beta;
+  const float* k2;  // two-record tokens: the second record's key, value and step
+  const float* v2;
+  const float* beta2;
   float* o;
   const float* S0;  // init source (NULL: zero)
   float* S_out;     // export target
@@ -92,6 +97,7 @@ struct Fp32Params {
 
 cudaError_t launch_init(const Params& p, cudaStream_t st);
 cudaError_t launch_append(const Params& p, cudaStream_t st);
+cudaError_t launch_append2(const Params& p, cudaStream_t st);
 cudaError_t launch_step(const Params& p, cudaStream_t st);
 cudaError_t launch_fold(const Params& p, cudaStream_t st);
 cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st);

@@ -289,7 +289,7 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 // when the keys travel in registers). The token's q, k, v (and alpha) are read
 // into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
-                                              bool append, bool fold, int bits, int comp_fit) {
+                                              bool append, bool fold, int bits, int comp_fit, bool two = false) {
   Stage L;
   int o = 0;
   auto take = [&](int bytes) {
@@ -321,6 +321,12 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.h = take(4 * (W + 1));
   L.ec = take(4 * (C > 0 ? C : 1));
   L.eq = take(4 * (C > 0 ? C : 1));
+  const int tw = two ? 1 : 0;
+  L.k2n_b = take(tw * 4 * kBV);
+  L.zk2_b = take(tw * 4 * kBV);
+  L.basek2 = take(tw * 4 * kD);
+  L.g2 = take(tw * 4 * (W + 1));
+  L.ec2 = take(tw * 4 * (C > 0 ? C : 1));
   L.end = o;
   return L;
 }
@@ -756,6 +762,316 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     if (FOLD) {
       ru[(n - 1) * kD + i] = u;
       at<float>(sm, L.rec_k)[(n - 1) * kD + i] = tk.k;
+    }
+  }
+}
+
+// Two-record token: records n (k1, u1, alpha) and n+1 (k2, u2, decay 1) of a
+// head-state holding n-1 records, and the output o = S_{n+1} q. LeapQuant
+// App. A: a token whose update takes two rank-one sub-steps leaves two records
+// (DeltaProduct with two steps: u1 = beta1 (v1 - S_{n-1}(alpha . k1)),
+// u2 = beta2 (v2 - S_n k2)). Every pinned quantity is what two appends in a
+// row compute: the second append's decay products equal the first's (P_n = 1,
+// and a product with decay 1 is exact), so one pass over the codes gives both
+// reads and the output -- three fma chains per code instead of two.
+// 128 threads: lane group (w, r) owns rows 16pp + 4w + r, pp = 0..7.
+template <bool KDA, bool B4, bool FIT>
+__device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
+                                                float alpha_scalar, float beta1, float beta2, const TokenRegs& tk,
+                                                float k2v, float v2v, const float4 (&kpre)[4]) {
+  constexpr int NW = 4, RPT = 8, NG = 16;
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float* P = at<float>(sm, L.P);
+  float* P_b = at<float>(sm, L.P_b);
+  float* kn_b = at<float>(sm, L.kn_b);
+  float* k2n_b = at<float>(sm, L.k2n_b);
+  float* qn_b = at<float>(sm, L.qn_b);
+  float* zk_b = at<float>(sm, L.zk_b);
+  float* zk2_b = at<float>(sm, L.zk2_b);
+  float* zq_b = at<float>(sm, L.zq_b);
+  float* basek = at<float>(sm, L.basek);
+  float* basek2 = at<float>(sm, L.basek2);
+  float* baseq = at<float>(sm, L.baseq);
+  float* g = at<float>(sm, L.g);
+  float* g2 = at<float>(sm, L.g2);
+  float* h = at<float>(sm, L.h);
+  float* ec = at<float>(sm, L.ec);
+  float* ec2 = at<float>(sm, L.ec2);
+  float* eq = at<float>(sm, L.eq);
+  const float* ra = at<float>(sm, L.rec_alpha);
+  const float* sg = at<float>(sm, L.sigma);
+  const float* lam = at<float>(sm, L.lambda);
+  const int32_t* cid = at<int32_t>(sm, L.comp_id);
+  const float* cl = at<float>(sm, L.comp_line);
+
+  // A0: the decay products of record n's append (P_n = 1, P_{m-1} = P_m alpha_m);
+  // record n+1 adds P_{n+1} = 1 and leaves the rest unchanged.
+  if (KDA) {
+    if (tid < kD) {
+      const int jb = bv(tid);
+      float pr = 1.0f;
+      P_b[n * kBV + jb] = pr;
+      for (int m = n; m >= 1; --m) {
+        pr = __fmul_rn(pr, m == n ? tk.a : ra[(m - 1) * kD + tid]);
+        P_b[(m - 1) * kBV + jb] = pr;
+      }
+    }
+  } else if (tid == 0) {
+    float al[kMaxW];
+#pragma unroll
+    for (int q4 = 0; q4 < kMaxW / 4; ++q4) {
+      if (4 * q4 < n - 1) {
+        const float4 a4 = *reinterpret_cast<const float4*>(ra + 4 * q4);
+        al[4 * q4] = a4.x;
+        al[4 * q4 + 1] = a4.y;
+        al[4 * q4 + 2] = a4.z;
+        al[4 * q4 + 3] = a4.w;
+      }
+    }
+    float pr = 1.0f;
+    P[n] = pr;
+    pr = __fmul_rn(pr, alpha_scalar);
+    P[n - 1] = pr;
+#pragma unroll
+    for (int m = kMaxW - 1; m >= 1; --m) {
+      if (m <= n - 1) {
+        pr = __fmul_rn(pr, al[m - 1]);
+        P[m - 1] = pr;
+      }
+    }
+  }
+  __syncthreads();
+  // A1: y1 = A . k1, y2 = A . k2, A . q and their smoothed forms.
+  if (tid < kD) {
+    const int j = tid, jb = bv(j);
+    const float A = KDA ? P_b[jb] : P[0];
+    kn_b[jb] = tk.k;
+    k2n_b[jb] = k2v;
+    qn_b[jb] = tk.q;
+    zk_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, tk.k));
+    zk2_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, k2v));
+    zq_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, tk.q));
+  }
+  __syncthreads();
+
+  // Dot products, one lane group each: records m = 1..n-1 against k1, k2 and q;
+  // the compensators against the three; record n (k1) against k2 and q; k2 . q.
+  {
+    const int grp = tid >> 3;
+    const int nrec = n - 1;
+    const int njobs = nrec + p.C + 2;
+    for (int base = 0; base < njobs; base += NG) {
+      const int job = base + grp;
+      float pa = 0.0f, pa2 = 0.0f, pb = 0.0f;
+      if (job < njobs) {
+        const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
+        const float4* k2x4 = reinterpret_cast<const float4*>(k2n_b + 20 * qq);
+        const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
+        if (job < nrec || job == nrec + p.C) {
+          // record m = job + 1 (held), or record n = (k1, P_n = 1) when job == nrec + C
+          const bool held = job < nrec;
+          const int m = held ? job + 1 : n;
+          float4 kv[4];
+          if (!held) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = kx4[c4];
+          } else if (base == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = kpre[c4];
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * p.W + job) * kD + 16 * qq);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = src[c4];
+          }
+          const float4* pm4 = reinterpret_cast<const float4*>(P_b + m * kBV + 20 * qq);
+          const float pms = KDA ? 0.0f : P[m];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 kvc = kv[c4], kx = kx4[c4], k2x = k2x4[c4], qx = qx4[c4];
+            const float kvs[4] = {kvc.x, kvc.y, kvc.z, kvc.w};
+            const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, k2s[4] = {k2x.x, k2x.y, k2x.z, k2x.w};
+            const float qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            float pmv[4] = {pms, pms, pms, pms};
+            if (KDA) {
+              const float4 pm = pm4[c4];
+              pmv[0] = pm.x;
+              pmv[1] = pm.y;
+              pmv[2] = pm.z;
+              pmv[3] = pm.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (held) pa = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], kxs[e]), pa);
+              pa2 = __fmaf_rn(kvs[e], __fmul_rn(pmv[e], k2s[e]), pa2);
+              pb = KDA ? __fmaf_rn(kvs[e], __fmul_rn(pmv[e], qxs[e]), pb)
+                       : __fmaf_rn(kvs[e], qxs[e], pb);  // GDN: scaled by P_m after the tree
+            }
+          }
+        } else if (job < nrec + p.C) {
+          const int c = job - nrec;
+          const int id = cid[c];
+          const float4* b4 = reinterpret_cast<const float4*>(cl + (FIT ? (2 * c + 1) * kD : c * kD) + 16 * qq);
+          const float4* a04 = reinterpret_cast<const float4*>(P_b + 20 * qq);
+          const float a0s = KDA ? 0.0f : P[0];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 bb = b4[c4], kx = kx4[c4], k2x = k2x4[c4], qx = qx4[c4];
+            float bs[4] = {bb.x, bb.y, bb.z, bb.w};
+            const float kxs[4] = {kx.x, kx.y, kx.z, kx.w}, k2s[4] = {k2x.x, k2x.y, k2x.z, k2x.w};
+            const float qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            float av[4] = {a0s, a0s, a0s, a0s};
+            if (KDA) {
+              const float4 a0 = a04[c4];
+              av[0] = a0.x;
+              av[1] = a0.y;
+              av[2] = a0.z;
+              av[3] = a0.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!FIT && id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
+              pa = __fmaf_rn(bs[e], __fmul_rn(av[e], kxs[e]), pa);
+              pa2 = __fmaf_rn(bs[e], __fmul_rn(av[e], k2s[e]), pa2);
+              pb = __fmaf_rn(bs[e], __fmul_rn(av[e], qxs[e]), pb);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 k2x = k2x4[c4], qx = qx4[c4];
+            pb = __fmaf_rn(k2x.x, qx.x, pb);
+            pb = __fmaf_rn(k2x.y, qx.y, pb);
+            pb = __fmaf_rn(k2x.z, qx.z, pb);
+            pb = __fmaf_rn(k2x.w, qx.w, pb);
+          }
+        }
+      }
+      pa = tree8(pa);
+      pa2 = tree8(pa2);
+      pb = tree8(pb);
+      if (job < njobs && qq == 0) {
+        if (job < nrec) {
+          g[job] = pa;
+          g2[job] = pa2;
+          h[job] = KDA ? pb : __fmul_rn(P[job + 1], pb);
+        } else if (job < nrec + p.C) {
+          ec[job - nrec] = pa;
+          ec2[job - nrec] = pa2;
+          eq[job - nrec] = pb;
+        } else if (job == nrec + p.C) {
+          g2[n - 1] = pa2;
+          h[n - 1] = KDA ? pb : __fmul_rn(P[n], pb);
+        } else {
+          h[n] = pb;
+        }
+      }
+    }
+  }
+
+  // Three chains per code: base terms of the two reads and of the output.
+  {
+    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
+    const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
+    const float4* zk24 = reinterpret_cast<const float4*>(zk2_b + 20 * qq);
+    const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
+    float v[2 * RPT], vq[RPT];
+#pragma unroll
+    for (int half = 0; half < RPT / 4; ++half) {
+      uint32_t cw[4][4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+        code_words<B4>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<B4>(), cw[pp]);
+      float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 x1 = zk4[c4], x2 = zk24[c4], xq = zq4[c4];
+        const float z1[4] = {x1.x, x1.y, x1.z, x1.w}, z2[4] = {x2.x, x2.y, x2.z, x2.w};
+        const float zq[4] = {xq.x, xq.y, xq.z, xq.w};
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f = code_at<B4>(cw[pp], 4 * c4 + e);
+            a1[pp] = __fmaf_rn(f, z1[e], a1[pp]);
+            a2[pp] = __fmaf_rn(f, z2[e], a2[pp]);
+            aq[pp] = __fmaf_rn(f, zq[e], aq[pp]);
+          }
+        }
+      }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        v[4 * half + pp] = a1[pp];
+        v[RPT + 4 * half + pp] = a2[pp];
+        vq[4 * half + pp] = aq[pp];
+      }
+    }
+    const int b0 = qq & 1, b1 = (qq >> 1) & 1, b2 = (qq >> 2) & 1;
+    float tot[2], totq[1];
+    tree_transpose<2 * RPT>(v, qq, tot);
+    tree_transpose<RPT>(vq, qq, totq);
+    // lane qq: quantities 8 b0 + 4 b1 + 2 b2 + e of (k1 rows, k2 rows), and q row 4 b0 + 2 b1 + b2
+    float* dst = b0 ? basek2 : basek;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = (4 * b1 + 2 * b2 + e) * 4 * NW + 4 * w + r;
+      dst[i] = __fmul_rn(sg[i], tot[e]);
+    }
+    const int iq = (4 * b0 + 2 * b1 + b2) * 4 * NW + 4 * w + r;
+    baseq[iq] = __fmul_rn(sg[iq], totq[0]);
+  }
+  __syncthreads();
+
+  // Rows: u1 from the first read; the second read adds record n (u1, k1) last;
+  // the output adds record n and then record n+1 (u2, k2 . q).
+  if (tid < kD) {
+    const int i = tid;
+    const float* ru = at<float>(sm, L.rec_u);
+    const int64_t rec_off = (s * p.W + (n - 1)) * kD;  // record slot n-1; slot n follows
+    float acc = basek[i], acc2 = basek2[i], oo = baseq[i];
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      if (c < p.C) {
+        const int id = cid[c];
+        const float a = FIT ? cl[2 * c * kD + i] : (id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f));
+        acc = __fmaf_rn(a, ec[c], acc);
+        acc2 = __fmaf_rn(a, ec2[c], acc2);
+        oo = __fmaf_rn(a, eq[c], oo);
+      }
+    }
+    const float* rui = ru + i;
+    for (int m0 = 0; m0 < n - 1; m0 += 4) {
+      const float4 g4 = *reinterpret_cast<const float4*>(g + m0);
+      const float4 g24 = *reinterpret_cast<const float4*>(g2 + m0);
+      const float4 h4 = *reinterpret_cast<const float4*>(h + m0);
+      const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, g2s[4] = {g24.x, g24.y, g24.z, g24.w};
+      const float hs[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (m0 + e < n - 1) {
+          const float um = rui[(m0 + e) * kD];
+          acc = __fmaf_rn(um, gs[e], acc);
+          acc2 = __fmaf_rn(um, g2s[e], acc2);
+          oo = __fmaf_rn(um, hs[e], oo);
+        }
+      }
+    }
+    const float u1 = __fmul_rn(beta1, __fsub_rn(tk.v, acc));
+    acc2 = __fmaf_rn(u1, g2[n - 1], acc2);
+    oo = __fmaf_rn(u1, h[n - 1], oo);
+    const float u2 = __fmul_rn(beta2, __fsub_rn(v2v, acc2));
+    oo = __fmaf_rn(u2, h[n], oo);
+    p.rec_u[rec_off + i] = u1;
+    p.rec_u[rec_off + kD + i] = u2;
+    p.rec_k[rec_off + i] = tk.k;
+    p.rec_k[rec_off + kD + i] = k2v;
+    p.o[s * kD + i] = oo;
+    if (KDA) {
+      p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + i] = tk.a;
+      p.rec_alpha[s * p.alpha_stride + n * kD + i] = 1.0f;
+    } else if (i == 0) {
+      p.rec_alpha[s * p.alpha_stride + (n - 1)] = alpha_scalar;
+      p.rec_alpha[s * p.alpha_stride + n] = 1.0f;
     }
   }
 }
@@ -1449,7 +1765,7 @@ __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int
 // checks. Returns the record count held (>= 0), or after recording an error -1
 // (the copies have landed) or -2 (the wait gave up); uniform over the CTA.
 __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t* bar, const StageInfo& si,
-                                            bool append, uint32_t parity = 0) {
+                                            bool append, uint32_t parity = 0, int room = 1) {
   const int n0 = si.issued, cnt = si.cnt;
   const bool hdr = si.hdr != 0;
   if (n0 >= 0) {
@@ -1465,7 +1781,7 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
     err = LQ_ERR_STATE;
   else if (append && p.phase >= 0 && cnt != p.phase)
     err = LQ_ERR_PHASE;
-  else if (append && cnt >= p.W)
+  else if (append && cnt + room > p.W)
     err = LQ_ERR_WINDOW_FULL;
   else if (cnt != n0)
     err = LQ_ERR_STATE;
@@ -1516,6 +1832,47 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 1;
     if (p.push_full && n0 + 1 == p.W) {
+      const int slot = atomicAdd(&p.hdr->full_n, 1);
+      if (slot >= 0 && slot < p.n_states)
+        p.full_list[slot] = (int32_t)s;
+      else
+        set_error(p, LQ_ERR_STATE, s);
+    }
+  }
+}
+
+// Two-record tokens (lq_decode_step2): records n and n+1 in one pass. Staging
+// holds the stated phase's records (W-2 when the phase is not stated).
+__host__ __device__ inline int append2_slots(int W, int phase) {
+  return (phase >= 0 && phase <= W - 2) ? phase : W - 2;
+}
+
+template <bool KDA, bool B4, bool FIT>
+__global__ void __launch_bounds__(128, 6) k_append2(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ StageInfo s_info;
+  const int64_t s = blockIdx.x;
+  const int slots = append2_slots(p.W, p.phase);
+  const Stage& L = p.st;
+  const float beta1 = p.beta[s], beta2 = p.beta2[s];
+  const float alpha_s = KDA ? 0.0f : p.alpha[s];
+  const int known = (p.phase >= 0 && p.phase <= p.W - 2) ? p.phase : -1;
+  const TokenRegs tk = load_token(p, s);
+  float k2v = 0.0f, v2v = 0.0f;
+  if (threadIdx.x < kD) {
+    k2v = p.k2[s * kD + threadIdx.x];
+    v2v = p.v2[s * kD + threadIdx.x];
+  }
+  float4 kpre[4];
+  if (known >= 0) prefetch_key(p, s, known, kpre);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
+  if (known < 0) prefetch_key(p, s, si.issued, kpre);
+  const int n0 = stage_finish(p, s, &bar, si, true, 0, 2);
+  if (n0 < 0) return;
+  append2_compute<KDA, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta1, beta2, tk, k2v, v2v, kpre);
+  if (threadIdx.x == 0) {
+    p.counts[s] = n0 + 2;
+    if (p.push_full && n0 + 2 == p.W) {
       const int slot = atomicAdd(&p.hdr->full_n, 1);
       if (slot >= 0 && slot < p.n_states)
         p.full_list[slot] = (int32_t)s;
@@ -1714,9 +2071,11 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
 // ---------------------------------------------------------------------------
 // launchers
 
-static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile) {
+static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile,
+                          bool two = false) {
   Params q = p;
-  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits, p.comp_fit);
+  q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits, p.comp_fit,
+                      two);
   q.r1 = tile ? region1_bytes(q.st) : q.st.end;
   return q;
 }
@@ -1767,6 +2126,11 @@ cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st) {
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, append_slots(p.W, p.phase), 0, true, false, false);
   return launch(LQ_PICK2(k_append, q), q, smem_of(q, false), st, 128);
+}
+
+cudaError_t launch_append2(const Params& p, cudaStream_t st) {
+  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true);
+  return launch(LQ_PICK2(k_append2, q), q, smem_of(q, false), st, 128);
 }
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {

@@ -29,8 +29,8 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
 
 # Every symbol include/lq.h declares.
 EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_state_init_range", "lq_append",
-           "lq_fold", "lq_decode_step", "lq_export_state", "lq_fp32_decode_step", "lq_get_status",
-           "lq_clear_status", "lq_last_error", "lq_version")
+           "lq_fold", "lq_decode_step", "lq_decode_step2", "lq_export_state", "lq_fp32_decode_step",
+           "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
 
 
 class Config(ctypes.Structure):
@@ -81,6 +81,7 @@ def load():
         "lq_append": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
         "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
+        "lq_decode_step2": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P, P, P, P]),
         "lq_export_state": (ctypes.c_int, [cfgp, P, i64, P, P]),
         "lq_fp32_decode_step": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_get_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), P]),
@@ -193,6 +194,15 @@ def decode_step(cfg, state, n_states, q, k, v, alpha, beta, o, phase=PHASE_ANY, 
     _check(load().lq_decode_step(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(phase), _ptr(q, "q", f),
                                  _ptr(k, "k", f), _ptr(v, "v", f), _ptr(alpha, "alpha", f), _ptr(beta, "beta", f),
                                  _ptr(o, "o", f), _stream(stream)))
+
+
+def decode_step2(cfg, state, n_states, q, k1, v1, beta1, k2, v2, beta2, alpha, o, phase=PHASE_ANY, stream=None):
+    """One two-record token (records (k1, u1, alpha) and (k2, u2, 1)); o = S_{n+1} q."""
+    f = _f32()
+    _check(load().lq_decode_step2(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(phase), _ptr(q, "q", f),
+                                  _ptr(k1, "k1", f), _ptr(v1, "v1", f), _ptr(beta1, "beta1", f), _ptr(k2, "k2", f),
+                                  _ptr(v2, "v2", f), _ptr(beta2, "beta2", f), _ptr(alpha, "alpha", f),
+                                  _ptr(o, "o", f), _stream(stream)))
 
 
 def export_state(cfg, state, n_states, S_out, stream=None):

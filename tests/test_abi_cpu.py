@@ -133,6 +133,12 @@ def test_invalid_sizes_and_nulls_rejected_on_host(L):
     # a bad phase is rejected before anything else is looked at
     assert L.lq_decode_step(ctypes.byref(cfg), None, 0, 16, None, None, None, None, None, None, None) == \
         lq.ERR_INVALID_ARG
+    step2 = lambda c, ph: L.lq_decode_step2(ctypes.byref(c), None, 0, ph, *([None] * 10))
+    assert step2(cfg, -1) == lq.OK and step2(cfg, 14) == lq.OK
+    assert step2(cfg, 15) == lq.ERR_INVALID_ARG  # no room for two records
+    one = lq.default_config()
+    one.window = 1
+    assert step2(one, -1) == lq.ERR_UNSUPPORTED
 
 
 def test_error_message_is_thread_local(L):
