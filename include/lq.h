@@ -71,7 +71,7 @@ typedef struct {
   int32_t decay_per_key; /* 0: scalar alpha per token (GDN); 1: alpha in R^{d_k} (KDA)      */
   int32_t smooth;        /* 1: residual smoothing on (default); 0: lambda = 1               */
   float lambda_floor;    /* positive floor of the smoothing scales (default 1e-6)           */
-  int32_t code_bits;     /* code width: 8 (default) or 4 ([LQ] §4 also evaluates 6- and      */
+  int32_t code_bits;     /* code width: 8 (default), 6 or 4 ([LQ] §4 also evaluates 6- and   */
                          /* 4-bit states); codes in [-q, q], q = 2^(bits-1) - 1              */
   int32_t comp_fit;      /* 0 (default): a compensator is an outlier line, kept exactly;     */
                          /* 1..32: a rank-one factor a b^T fitted to the residual by that   */
@@ -87,6 +87,12 @@ typedef struct {
  *   codes    int8    [s][d_v][d_k]             row-major (8-bit codes), or
  *            uint8   [s][d_v][d_k / 2]         4-bit codes: two per byte, code 2j in the
  *                                              low nibble, each stored as c + 8 (1..15)
+ *            uint8   [s][d_v][3 d_k / 4]       6-bit codes, each stored as c + 32 (1..63):
+ *                                              per row, 64 bytes of low nibbles laid out
+ *                                              as a 4-bit row, then 32 bytes holding the
+ *                                              top two bits: for element e of 16-code
+ *                                              block j, bits 8b + 2g of 32-bit word j,
+ *                                              g = 2(e/8) + (e mod 2), b = (e mod 8) / 2
  *   sigma    fp32    [s][d_v]                  quantization step of each value row
  *   lambda   fp32    [s][d_k]                  smoothing scale of each key channel
  *   comp_id  int32   [s][comp_id_stride]       id < d_v: row id; else column id - d_v

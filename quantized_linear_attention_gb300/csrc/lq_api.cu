@@ -56,10 +56,10 @@ int check_cfg(const lq_config* c) {
     return fail(LQ_ERR_INVALID_ARG, "lambda_floor must be finite and > 0");
   if (c->comp_fit < 0 || c->comp_fit > 32)
     return fail(LQ_ERR_INVALID_ARG, "comp_fit must be 0..32 (got %d)", c->comp_fit);
-  if (c->code_bits != 8 && c->code_bits != 4) {
+  if (c->code_bits != 8 && c->code_bits != 6 && c->code_bits != 4) {
     if (c->code_bits >= 2 && c->code_bits <= 7)
-      return fail(LQ_ERR_UNSUPPORTED, "code_bits %d: this build runs 8- and 4-bit codes", c->code_bits);
-    return fail(LQ_ERR_INVALID_ARG, "code_bits must be 8 or 4 (got %d)", c->code_bits);
+      return fail(LQ_ERR_UNSUPPORTED, "code_bits %d: this build runs 8-, 6- and 4-bit codes", c->code_bits);
+    return fail(LQ_ERR_INVALID_ARG, "code_bits must be 8, 6 or 4 (got %d)", c->code_bits);
   }
   return LQ_OK;
 }

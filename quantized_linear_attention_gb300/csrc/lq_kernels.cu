@@ -96,44 +96,55 @@ __device__ __forceinline__ f32x2 code_pair(uint32_t w_lo, int b_lo, uint32_t w_h
 }
 
 // A lane's 16 codes of one row as four words of biased bytes, and the exact
-// conversion of code e (0..15) from them.
-//  8-bit codes (int8, 16 bytes): the words are the four code words with every
-//    byte biased by ^0x80 (c + 128).
-//  4-bit codes (8 bytes, nibble e of the block holds c + 8, low nibble first):
-//    the words are {lo0, hi0, lo1, hi1}, the even and odd nibbles of the two
-//    code words spread into bytes; element e sits in word 2(e/8) + (e & 1),
-//    byte (e & 7) / 2.
-// Each byte goes into the mantissa of 2^23 and the bias 2^23 + 128 (or 2^23 + 8)
+// conversion of code e (0..15) from them. Row layouts (one row = d_k codes):
+//  8-bit (128 B): int8 codes; lane qq's block is bytes 16qq..16qq+15, and the
+//    words are its four code words with every byte biased by ^0x80 (c + 128).
+//  4-bit (64 B): nibble e of the block (bytes 8qq..8qq+7) holds c + 8, low
+//    nibble first; the words are {lo0, hi0, lo1, hi1}, the even and odd nibbles
+//    of the two code words spread into bytes, so element e sits in word
+//    g = 2(e/8) + (e & 1), byte b = (e & 7) / 2.
+//  6-bit (96 B): c + 32 (1..63); its low nibble in a 64-byte nibble plane laid
+//    out as the 4-bit row, its top two bits in a 32-byte plane after it. Word qq
+//    of that plane holds element e's bits at 8b + 2g (g, b as above), so one
+//    shift and one mask put them at bits 4-5 of the byte the nibble went to.
+// Each byte goes into the mantissa of 2^23 and the bias 2^23 + 128 (+ 8, + 32)
 // is subtracted: both steps are exact.
-template <bool B4>
-__device__ __forceinline__ void code_words(const int8_t* row_block, uint32_t cw[4]) {
-  if (B4) {
-    const uint2 c = *reinterpret_cast<const uint2*>(row_block);
-    cw[0] = c.x & 0x0F0F0F0Fu;
-    cw[1] = (c.x >> 4) & 0x0F0F0F0Fu;
-    cw[2] = c.y & 0x0F0F0F0Fu;
-    cw[3] = (c.y >> 4) & 0x0F0F0F0Fu;
-  } else {
-    const int4 c = *reinterpret_cast<const int4*>(row_block);
+template <int BITS>
+__device__ __forceinline__ void code_words(const int8_t* row, int qq, uint32_t cw[4]) {
+  if (BITS == 8) {
+    const int4 c = *reinterpret_cast<const int4*>(row + 16 * qq);
     cw[0] = (uint32_t)c.x ^ 0x80808080u;
     cw[1] = (uint32_t)c.y ^ 0x80808080u;
     cw[2] = (uint32_t)c.z ^ 0x80808080u;
     cw[3] = (uint32_t)c.w ^ 0x80808080u;
+  } else {
+    const uint2 c = *reinterpret_cast<const uint2*>(row + 8 * qq);
+    cw[0] = c.x & 0x0F0F0F0Fu;
+    cw[1] = (c.x >> 4) & 0x0F0F0F0Fu;
+    cw[2] = c.y & 0x0F0F0F0Fu;
+    cw[3] = (c.y >> 4) & 0x0F0F0F0Fu;
+    if (BITS == 6) {
+      const uint32_t hw = *reinterpret_cast<const uint32_t*>(row + 64 + 4 * qq);
+      cw[0] |= (hw << 4) & 0x30303030u;
+      cw[1] |= (hw << 2) & 0x30303030u;
+      cw[2] |= hw & 0x30303030u;
+      cw[3] |= (hw >> 2) & 0x30303030u;
+    }
   }
 }
 
-template <bool B4>
+template <int BITS>
 __device__ __forceinline__ float code_at(const uint32_t cw[4], int e) {
-  const uint32_t w = B4 ? cw[2 * (e >> 3) + (e & 1)] : cw[e >> 2];
-  const int b = B4 ? ((e & 7) >> 1) : (e & 3);
+  const uint32_t w = BITS == 8 ? cw[e >> 2] : cw[2 * (e >> 3) + (e & 1)];
+  const int b = BITS == 8 ? (e & 3) : ((e & 7) >> 1);
   const uint32_t bits = __byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)b);
-  return __fsub_rn(__uint_as_float(bits), B4 ? 8388616.0f : 8388736.0f);
+  return __fsub_rn(__uint_as_float(bits), BITS == 8 ? 8388736.0f : (BITS == 6 ? 8388640.0f : 8388616.0f));
 }
 
-// Bytes of one row of codes, and of one lane's 16-code block.
-template <bool B4>
+// Bytes of one row of codes.
+template <int BITS>
 __host__ __device__ constexpr int row_bytes() {
-  return B4 ? kD / 2 : kD;
+  return kD * BITS / 8;
 }
 
 // Sum of the 8 block partials of a lane group in the fixed tree order.
@@ -475,7 +486,7 @@ __device__ __forceinline__ TokenRegs load_token(const Params& p, int64_t s) {
 // KPRE: record keys are not staged; lane group g arrives with block qq of
 // record slot g in `kpre` (read before the staging wait), and slots beyond the
 // first round of lane groups are read from global memory.
-template <bool KDA, int NT, bool FOLD, bool KPRE, bool B4, bool FIT>
+template <bool KDA, int NT, bool FOLD, bool KPRE, int BITS, bool FIT>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                float alpha_scalar, float beta, const TokenRegs& tk,
                                                const float4 (&kpre)[4]) {
@@ -671,7 +682,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   // time, 4 rows interleaved; each row's chain runs over its 16 elements in
   // ascending order, then the canonical tree (shared out over the lane group).
   {
-    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
+    const int8_t* cb = at<int8_t>(sm, L.codes);
     const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
     const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
     float v[2 * RPT];
@@ -680,7 +691,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       uint32_t cw[4][4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp)
-        code_words<B4>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<B4>(), cw[pp]);
+        code_words<BITS>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<BITS>(), qq, cw[pp]);
       float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -690,7 +701,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         for (int pp = 0; pp < 4; ++pp) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float f = code_at<B4>(cw[pp], 4 * c4 + e);
+            const float f = code_at<BITS>(cw[pp], 4 * c4 + e);
             ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
             aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
           }
@@ -775,7 +786,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
 // and a product with decay 1 is exact), so one pass over the codes gives both
 // reads and the output -- three fma chains per code instead of two.
 // 128 threads: lane group (w, r) owns rows 16pp + 4w + r, pp = 0..7.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                 float alpha_scalar, float beta1, float beta2, const TokenRegs& tk,
                                                 float k2v, float v2v, const float4 (&kpre)[4]) {
@@ -971,7 +982,7 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
 
   // Three chains per code: base terms of the two reads and of the output.
   {
-    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
+    const int8_t* cb = at<int8_t>(sm, L.codes);
     const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
     const float4* zk24 = reinterpret_cast<const float4*>(zk2_b + 20 * qq);
     const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
@@ -981,7 +992,7 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
       uint32_t cw[4][4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp)
-        code_words<B4>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<B4>(), cw[pp]);
+        code_words<BITS>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<BITS>(), qq, cw[pp]);
       float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -992,7 +1003,7 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
         for (int pp = 0; pp < 4; ++pp) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float f = code_at<B4>(cw[pp], 4 * c4 + e);
+            const float f = code_at<BITS>(cw[pp], 4 * c4 + e);
             a1[pp] = __fmaf_rn(f, z1[e], a1[pp]);
             a2[pp] = __fmaf_rn(f, z2[e], a2[pp]);
             aq[pp] = __fmaf_rn(f, zq[e], aq[pp]);
@@ -1141,7 +1152,7 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
 // F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
 // lambda_j) P_0[j], then the compensators in order, then the records in order,
 // each an fma. Adjacent columns (2k, 2k+1) of a row travel as one packed pair.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1158,16 +1169,16 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
     // the 32 accumulator pairs.
     const float* lam = at<float>(sm, L.lam_b) + 20 * qq;
     const float* p0b = P_b + 20 * qq;
-    const int8_t* cb = at<int8_t>(sm, L.codes) + (B4 ? 8 : 16) * qq;
+    const int8_t* cb = at<int8_t>(sm, L.codes);
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int i = 32 * pp + 4 * w + r;
       const float s_i = sg[i];
       uint32_t cw[4];
-      code_words<B4>(cb + i * row_bytes<B4>(), cw);
+      code_words<BITS>(cb + i * row_bytes<BITS>(), qq, cw);
       float f[16];
 #pragma unroll
-      for (int t = 0; t < 16; ++t) f[t] = code_at<B4>(cw, t);
+      for (int t = 0; t < 16; ++t) f[t] = code_at<BITS>(cw, t);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float2 l2 = *reinterpret_cast<const float2*>(lam + 2 * k);
@@ -1509,7 +1520,7 @@ __device__ __forceinline__ void fit_factors_tile(const Params& p, int64_t s, flo
 }
 
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
-template <bool B4, bool FIT>
+template <int BITS, bool FIT>
 __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1644,7 +1655,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
   {
     float g[16];
     load16(tl.gsc_b + 20 * qq, g);
-    int8_t* cbase = p.codes + s * (kD * row_bytes<B4>()) + (B4 ? 8 : 16) * qq;
+    int8_t* cbase = p.codes + s * (kD * row_bytes<BITS>());
     int roff[4];
     row_offsets(4 * w + r, qq, roff);
     float t[4][16], mx[4];
@@ -1677,9 +1688,9 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     }
     float m1 = fmaxf(b1 ? m2[1] : m2[0], __shfl_xor_sync(0xffffffffu, b1 ? m2[0] : m2[1], 2));
     m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 4));
-    // sigma = m / q and the reciprocal h = q / m, once per row (q = 127 for
-    // 8-bit codes, 7 for 4-bit ones); zero row: 0, 0.
-    constexpr float q = B4 ? 7.0f : 127.0f;
+    // sigma = m / q and the reciprocal h = q / m, once per row (q = 127, 31 or
+    // 7 for 8-, 6- or 4-bit codes); zero row: 0, 0.
+    constexpr float q = BITS == 8 ? 127.0f : (BITS == 6 ? 31.0f : 7.0f);
     float sgm = 0.0f, hown = 0.0f;
     if (m1 != 0.0f) {
       sgm = __fdiv_rn(m1, q);
@@ -1693,28 +1704,42 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
       const float hh = __shfl_sync(0xffffffffu, hown, (lane & ~7) | ((pp >> 1) | ((pp & 1) << 1)));
       const int i = 32 * pp + 4 * w + r;
       // Round t*h to the nearest integer, ties to even: |t*h| <= q(1+2^-24)^2 <
-      // q + 1/2 (q = 127 or 7), so adding 1.5 * 2^23 leaves the integer, in
-      // [-q, q], in the low mantissa bits (two's complement), and no clamp is
-      // needed. For 4-bit codes the added constant carries the +8 bias too, so
-      // the low nibble is c + 8 (1..15).
+      // q + 1/2, so adding 1.5 * 2^23 leaves the integer, in [-q, q], in the
+      // low mantissa bits (two's complement), and no clamp is needed. For 6- and
+      // 4-bit codes the added constant carries the bias (+32, +8) too, so the
+      // low bits hold c + 32 (1..63) or c + 8 (1..15).
+      constexpr float magic = BITS == 8 ? 12582912.0f : (BITS == 6 ? 12582944.0f : 12582920.0f);
       uint32_t rb[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[pp][e], hh), B4 ? 12582920.0f : 12582912.0f));
-      if (B4) {
-        uint32_t v[8];  // byte 0 of v[k]: codes 2k (low nibble) and 2k + 1
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = rb[2 * k] | (rb[2 * k + 1] << 4);
-        const uint32_t w0 = __byte_perm(__byte_perm(v[0], v[1], 0x0040u), __byte_perm(v[2], v[3], 0x0040u), 0x5410u);
-        const uint32_t w1 = __byte_perm(__byte_perm(v[4], v[5], 0x0040u), __byte_perm(v[6], v[7], 0x0040u), 0x5410u);
-        *reinterpret_cast<uint2*>(cbase + i * row_bytes<B4>()) = make_uint2(w0, w1);
-      } else {
+      for (int e = 0; e < 16; ++e) rb[e] = __float_as_uint(__fadd_rn(__fmul_rn(t[pp][e], hh), magic));
+      int8_t* row = cbase + i * row_bytes<BITS>();
+      if (BITS == 8) {
         uint32_t wd[4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
           wd[q4] = __byte_perm(__byte_perm(rb[4 * q4], rb[4 * q4 + 1], 0x0040u),
                                __byte_perm(rb[4 * q4 + 2], rb[4 * q4 + 3], 0x0040u), 0x5410u);
-        *reinterpret_cast<int4*>(cbase + i * kD) = make_int4((int)wd[0], (int)wd[1], (int)wd[2], (int)wd[3]);
+        *reinterpret_cast<int4*>(row + 16 * qq) = make_int4((int)wd[0], (int)wd[1], (int)wd[2], (int)wd[3]);
+      } else {
+        uint32_t v[8];  // byte 0 of v[k]: the low nibbles of codes 2k and 2k + 1
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = (rb[2 * k] & 0x0Fu) | ((rb[2 * k + 1] & 0x0Fu) << 4);
+        const uint32_t w0 = __byte_perm(__byte_perm(v[0], v[1], 0x0040u), __byte_perm(v[2], v[3], 0x0040u), 0x5410u);
+        const uint32_t w1 = __byte_perm(__byte_perm(v[4], v[5], 0x0040u), __byte_perm(v[6], v[7], 0x0040u), 0x5410u);
+        *reinterpret_cast<uint2*>(row + 8 * qq) = make_uint2(w0, w1);
+        if (BITS == 6) {
+          // word g of the spread has byte b = element 8(g/2) + 2b + (g&1); its
+          // top two bits go to bits 8b + 2g of the high word
+          uint32_t hw = 0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int e0 = 8 * (g >> 1) + (g & 1);
+            const uint32_t wg = __byte_perm(__byte_perm(rb[e0], rb[e0 + 2], 0x0040u),
+                                            __byte_perm(rb[e0 + 4], rb[e0 + 6], 0x0040u), 0x5410u);
+            hw |= ((wg >> 4) & 0x03030303u) << (2 * g);
+          }
+          *reinterpret_cast<uint32_t*>(row + 64 + 4 * qq) = hw;
+        }
       }
     }
   }
@@ -1811,7 +1836,7 @@ __device__ __forceinline__ void prefetch_key(const Params& p, int64_t s, int n0,
 // into registers before the staging wait -- at once when the phase is stated,
 // else once thread 0 has read the record count. With p.push_full the
 // head-states whose window this token fills are put on the full-window list.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1828,7 +1853,7 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   if (known < 0) prefetch_key(p, s, si.issued, kpre);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false, true, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 128, false, true, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 1;
     if (p.push_full && n0 + 1 == p.W) {
@@ -1847,7 +1872,7 @@ __host__ __device__ inline int append2_slots(int W, int phase) {
   return (phase >= 0 && phase <= W - 2) ? phase : W - 2;
 }
 
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1869,7 +1894,7 @@ __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
   if (known < 0) prefetch_key(p, s, si.issued, kpre);
   const int n0 = stage_finish(p, s, &bar, si, true, 0, 2);
   if (n0 < 0) return;
-  append2_compute<KDA, B4, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta1, beta2, tk, k2v, v2v, kpre);
+  append2_compute<KDA, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta1, beta2, tk, k2v, v2v, kpre);
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 2;
     if (p.push_full && n0 + 2 == p.W) {
@@ -1883,7 +1908,7 @@ __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
 }
 
 // Append, then -- when that fills the window -- fold while the state is on chip.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1899,24 +1924,24 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   if (n0 < 0) return;
   const int n = n0 + 1;
   if (n < p.W) {
-    append_compute<KDA, 256, false, false, B4, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+    append_compute<KDA, 256, false, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  append_compute<KDA, 256, true, false, B4, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 256, true, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, BITS, FIT>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4, FIT>(p, s, S, tl);
+  boundary_from_tile<BITS, FIT>(p, s, S, tl);
 }
 
 // F0-F6 on a staged head-state holding n records.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __device__ __forceinline__ void fold_staged(const Params& p, int64_t s, int n) {
   const Stage& L = p.st;
   decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
@@ -1924,16 +1949,16 @@ __device__ __forceinline__ void fold_staged(const Params& p, int64_t s, int n) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, BITS, FIT>(p, n, L, lq_dyn_smem, acc);
   __syncthreads();
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4, FIT>(p, s, S, tl);
+  boundary_from_tile<BITS, FIT>(p, s, S, tl);
 }
 
 // Fold with the records held (any count 0..W): lq_fold.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1941,7 +1966,7 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
   const StageInfo si = stage_start(p, s, -1, p.st, &bar, &s_info, true, p.W);
   const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
-  fold_staged<KDA, B4, FIT>(p, s, n);
+  fold_staged<KDA, BITS, FIT>(p, s, n);
 }
 
 // Fold the head-states on the full-window list (the second kernel of a
@@ -1949,7 +1974,7 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
 // b + 2G, ... (G = gridDim.x, at most the CTAs that fit on the GPU at once),
 // so the few head-states whose window fills this token are spread over every
 // SM. Each entry must hold W records. The last CTA to finish empties the list.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -1981,7 +2006,7 @@ __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
     const int n = stage_finish(p, s, &bar, si, false, parity);
     parity ^= 1u;
     if (n == -2) break;  // copies may still land: the barrier is not reused
-    if (n == p.W) fold_staged<KDA, B4, FIT>(p, s, n);
+    if (n == p.W) fold_staged<KDA, BITS, FIT>(p, s, n);
     else if (n >= 0 && threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
     __syncthreads();  // the next entry's copies overwrite what this one read
   }
@@ -1995,7 +2020,7 @@ __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
 }
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
-template <bool KDA, bool B4, bool FIT>
+template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -2011,7 +2036,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
-  reconstruct_rows<KDA, B4, FIT>(p, n, L, lq_dyn_smem, acc);
+  reconstruct_rows<KDA, BITS, FIT>(p, n, L, lq_dyn_smem, acc);
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
@@ -2025,7 +2050,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
 // Init-fold: F2-F6 on S0 (or zero). The whole buffer (p.first < 0): block 0
 // writes the header. A range (p.first >= 0): block b re-initialises head-state
 // first + b from S0 row block b, and the header must already match.
-template <bool B4, bool FIT>
+template <int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   __shared__ int s_ok;
   const bool range = p.first >= 0;
@@ -2065,7 +2090,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
   tile_store_rows(S, tl, acc);
-  boundary_from_tile<B4, FIT>(p, s, S, tl);
+  boundary_from_tile<BITS, FIT>(p, s, S, tl);
 }
 
 // ---------------------------------------------------------------------------
@@ -2103,8 +2128,10 @@ static cudaError_t init_any(const Params& p, int64_t grid, cudaStream_t st) {
   const int smem = smem_of(q, true);
   const bool fit = p.comp_fit > 0;
   if (p.bits == 4)
-    return fit ? launch(k_init<true, true>, q, smem, st, 256, grid) : launch(k_init<true, false>, q, smem, st, 256, grid);
-  return fit ? launch(k_init<false, true>, q, smem, st, 256, grid) : launch(k_init<false, false>, q, smem, st, 256, grid);
+    return fit ? launch(k_init<4, true>, q, smem, st, 256, grid) : launch(k_init<4, false>, q, smem, st, 256, grid);
+  if (p.bits == 6)
+    return fit ? launch(k_init<6, true>, q, smem, st, 256, grid) : launch(k_init<6, false>, q, smem, st, 256, grid);
+  return fit ? launch(k_init<8, true>, q, smem, st, 256, grid) : launch(k_init<8, false>, q, smem, st, 256, grid);
 }
 
 cudaError_t launch_init(const Params& p, cudaStream_t st) {
@@ -2115,10 +2142,10 @@ cudaError_t launch_init(const Params& p, cudaStream_t st) {
 
 cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st) { return init_any(p, count, st); }
 
-// Kernel K<KDA, B4, FIT> for this configuration's decay form, code width and compensator form.
+// Kernel K<KDA, BITS, FIT> for this configuration's decay form, code width and compensator form.
+#define LQ_PICK_F(K, q, KDA_, BITS_) ((q).comp_fit > 0 ? K<KDA_, BITS_, true> : K<KDA_, BITS_, false>)
 #define LQ_PICK_B(K, q, KDA_) \
-  ((q).bits == 4 ? ((q).comp_fit > 0 ? K<KDA_, true, true> : K<KDA_, true, false>) \
-                 : ((q).comp_fit > 0 ? K<KDA_, false, true> : K<KDA_, false, false>))
+  ((q).bits == 4 ? LQ_PICK_F(K, q, KDA_, 4) : ((q).bits == 6 ? LQ_PICK_F(K, q, KDA_, 6) : LQ_PICK_F(K, q, KDA_, 8)))
 #define LQ_PICK2(K, q) ((q).kda ? LQ_PICK_B(K, q, true) : LQ_PICK_B(K, q, false))
 
 // Staging holds `phase` records (W-1 when the phase is not stated); the keys
@@ -2167,5 +2194,6 @@ cudaError_t launch_export(const Params& p, cudaStream_t st) {
 
 #undef LQ_PICK2
 #undef LQ_PICK_B
+#undef LQ_PICK_F
 
 }  // namespace lqi

@@ -233,8 +233,8 @@ def clear_status(state, stream=None):
 
 def state_views(cfg: Config, state, n_states: int) -> dict:
     """Typed torch views of the planes of a state buffer (no copy), per ``lq_layout``. With
-    4-bit codes, "codes" is the packed plane: uint8 [N][d_v][d_k / 2], two codes per
-    byte (low nibble first), each stored as c + 8."""
+    4- or 6-bit codes, "codes" is the packed plane, uint8 [N][d_v][d_k * bits / 8]
+    (the layout ``include/lq.h`` gives)."""
     import torch
 
     L = layout(cfg, n_states)
@@ -247,7 +247,7 @@ def state_views(cfg: Config, state, n_states: int) -> dict:
     return {
         "counts": view(L.counts, N, torch.int32, (N,)),
         "codes": (view(L.codes, N * D * D, torch.int8, (N, D, D)) if cfg.code_bits == 8 else
-                  view(L.codes, N * D * D // 2, torch.uint8, (N, D, D // 2))),
+                  view(L.codes, N * D * D * cfg.code_bits // 8, torch.uint8, (N, D, D * cfg.code_bits // 8))),
         "sigma": view(L.sigma, N * D, torch.float32, (N, D)),
         "lambda": view(L.lambda_, N * D, torch.float32, (N, D)),
         "comp_id": view(L.comp_id, N * L.comp_id_stride, torch.int32, (N, L.comp_id_stride))[:, :C],

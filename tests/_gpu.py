@@ -17,10 +17,23 @@ def to_dev(x):
 
 
 def unpack_codes(codes):
-    """Code values (int8) from the codes plane: as is for 8-bit codes; for 4-bit
-    codes, two per byte (low nibble first), each stored as c + 8."""
+    """Code values (int8) from the codes plane: as is for 8-bit codes; 4-bit codes
+    are two per byte (low nibble first), each stored as c + 8; 6-bit codes (96-byte
+    rows) are stored as c + 32, low nibbles as a 4-bit row, then the top two bits of
+    element e of block j at bits 8b + 2g of word j (g = 2(e//8) + e%2, b = (e%8)//2)."""
     if codes.dtype == np.int8:
         return codes
+    if codes.shape[-1] == 96:
+        nib = codes[..., :64]
+        val = np.empty(codes.shape[:-1] + (128,), np.int16)
+        val[..., 0::2] = nib & 0x0F
+        val[..., 1::2] = nib >> 4
+        hw = codes[..., 64:].copy().view("<u4")  # [..., 16-code block j]
+        e = np.arange(16)
+        shift = 8 * ((e % 8) // 2) + 2 * (2 * (e // 8) + e % 2)
+        top = (hw[..., :, None] >> shift) & 3  # [..., j, e]
+        val += (top.reshape(val.shape) << 4).astype(np.int16)
+        return (val - 32).astype(np.int8)
     lo = (codes & 0x0F).astype(np.int16) - 8
     hi = (codes >> 4).astype(np.int16) - 8
     out = np.empty(codes.shape[:-1] + (2 * codes.shape[-1],), np.int8)

@@ -64,6 +64,16 @@ def test_boundary_bytes_with_4bit_codes(L):
     assert l4.sigma - l4.codes == 1000 * 8192
 
 
+def test_boundary_bytes_with_6bit_codes(L):
+    """6-bit codes (LeapQuant §4 also evaluates 6-bit states): 96 bytes per row, so
+    the boundary takes 12288 + 512 + 512 + 4C + 512C bytes, 0.94 per element."""
+    lay = lq.layout(lq.config(code_bits=6), 1)
+    assert lay.boundary_bytes_per_state == 12288 + 512 + 512 + 4 * 4 + 4 * 512 == 15376
+    assert round(lay.boundary_bytes_per_state / (128 * 128), 2) == 0.94
+    l6 = lq.layout(lq.config(code_bits=6), 1000)
+    assert l6.sigma - l6.codes == 1000 * 12288
+
+
 def test_fitted_factor_compensators_double_the_compensator_plane(L):
     """With comp_fit > 0 each compensator is a factor pair a (d_v) and b (d_k)."""
     l0 = lq.layout(lq.config(), 1)
@@ -100,7 +110,8 @@ def test_layout_planes(L, n, kda):
     ("window", 33, lq.ERR_UNSUPPORTED), ("n_comp", 9, lq.ERR_UNSUPPORTED), ("n_comp", -1, lq.ERR_UNSUPPORTED),
     ("decay_per_key", 2, lq.ERR_INVALID_ARG), ("smooth", 3, lq.ERR_INVALID_ARG),
     ("lambda_floor", 0.0, lq.ERR_INVALID_ARG), ("lambda_floor", float("inf"), lq.ERR_INVALID_ARG),
-    ("code_bits", 6, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG), ("code_bits", 0, lq.ERR_INVALID_ARG),
+    ("code_bits", 5, lq.ERR_UNSUPPORTED), ("code_bits", 7, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG),
+    ("code_bits", 0, lq.ERR_INVALID_ARG),
     ("comp_fit", -1, lq.ERR_INVALID_ARG), ("comp_fit", 33, lq.ERR_INVALID_ARG)])
 def test_invalid_config_rejected(L, field, value, code):
     cfg = lq.default_config()
