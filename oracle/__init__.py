@@ -8,4 +8,4 @@ It shares no code with the CUDA path.
 
 Every function is pinned by the CPU tests in ``tests/test_oracle_pins.py``.
 """
-from .oracle import FoldDiag, OracleState, dot, fp32_run, lib, sum_abs  # noqa: F401
+from .oracle import FoldDiag, OracleState, dot, fit, fp32_run, lib, sum_abs  # noqa: F401

@@ -61,6 +61,9 @@ typedef struct {
                          /* s > 0: rank-one factors (a, b) fitted by s sweeps of */
                          /* power iteration from the longest row ([RN4] "Where   */
                          /* the time goes"; [LQ] App. B.3 "fitting new factors") */
+  int32_t comp_block;    /* with comp_fit > 0: 1 fits the C factors together as  */
+                         /* a block from the previous window's factors ([RN4]    */
+                         /* "Redesign"); 0 one at a time as above                */
 } orc_cfg;
 
 /* Batch storage; every array holds n_states consecutive per-state blocks. */
@@ -384,7 +387,80 @@ static void fit_factors(const orc_cfg* cfg, float* R, orc_view st) {
   free(b);
 }
 
-static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st, orc_diag* dg) {
+/* v <- v - d u with d = dot(v, u), each entry by fma (one Gram-Schmidt step). */
+static void project_out(int d, float* v, const float* u) {
+  const float dp = orc_dot(d, v, 1, u, 1);
+  for (int j = 0; j < d; ++j) v[j] = fmaf(-dp, u[j], v[j]);
+}
+
+/* Modified Gram-Schmidt over the C vectors of V [C][d] in order: each vector
+ * loses its components along the earlier ones, then is normalized. */
+static void orthonormalize(int C, int d, float* V) {
+  for (int c = 0; c < C; ++c) {
+    for (int e = 0; e < c; ++e) project_out(d, V + (size_t)c * d, V + (size_t)e * d);
+    normalize(d, V + (size_t)c * d);
+  }
+}
+
+/*
+ * F2, block fit of the C factors ([RN4] "Redesign": fit the compensators
+ * together as a block, starting from the previous window's compensators; its
+ * counterexample: a block fit captures the strongest pattern where a start
+ * from the longest row misses it). Subspace iteration on the residual R:
+ *   start: v_c = the previous window's b_c when `prev` is given and b_c is not
+ *          zero, else the c-th longest row of R (squared length, ties to the
+ *          smaller row);
+ *   s sweeps of: orthonormalize V; v_c = R^T (R v_c) for every c;
+ *   orthonormalize V; then for c = 0..C-1: a_c = R v_c on the residual left
+ *   by the factors before it, store (a_c, v_c), deflate R_ij = fma(-a_c[i], v_c[j], R_ij).
+ * Every product sum is a dot in the fixed order; the compensator id is c.
+ */
+static void fit_block(const orc_cfg* cfg, float* R, orc_view st, const float* prev) {
+  const int dk = cfg->dk, dv = cfg->dv, C = cfg->C;
+  if (C <= 0) return;
+  float* V = (float*)malloc(sizeof(float) * (size_t)C * dk);
+  float* y = (float*)malloc(sizeof(float) * dv);
+  float* score = (float*)malloc(sizeof(float) * dv);
+  int* taken = (int*)calloc((size_t)dv, sizeof(int));
+  for (int i = 0; i < dv; ++i) score[i] = orc_dot(dk, R + (size_t)i * dk, 1, R + (size_t)i * dk, 1);
+  for (int c = 0; c < C; ++c) {
+    /* the c-th longest row (used where no previous factor is given) */
+    int best = -1;
+    for (int i = 0; i < dv; ++i)
+      if (!taken[i] && (best < 0 || score[i] > score[best])) best = i;
+    taken[best] = 1;
+    const float* b_prev = prev ? prev + (size_t)c * comp_len(cfg) + dv : NULL;
+    int nonzero = 0;
+    if (b_prev)
+      for (int j = 0; j < dk; ++j) nonzero |= b_prev[j] != 0.0f;
+    memcpy(V + (size_t)c * dk, nonzero ? b_prev : R + (size_t)best * dk, sizeof(float) * dk);
+  }
+  for (int sweep = 0; sweep < cfg->comp_fit; ++sweep) {
+    orthonormalize(C, dk, V);
+    for (int c = 0; c < C; ++c) {
+      float* v = V + (size_t)c * dk;
+      for (int i = 0; i < dv; ++i) y[i] = orc_dot(dk, R + (size_t)i * dk, 1, v, 1);
+      for (int j = 0; j < dk; ++j) v[j] = orc_dot(dv, R + j, dk, y, 1);
+    }
+  }
+  orthonormalize(C, dk, V);
+  for (int c = 0; c < C; ++c) {
+    const float* v = V + (size_t)c * dk;
+    for (int i = 0; i < dv; ++i) y[i] = orc_dot(dk, R + (size_t)i * dk, 1, v, 1);
+    float* out = st.comp_line + (size_t)c * comp_len(cfg);
+    memcpy(out, y, sizeof(float) * dv);
+    memcpy(out + dv, v, sizeof(float) * dk);
+    st.comp_id[c] = c;
+    for (int i = 0; i < dv; ++i)
+      for (int j = 0; j < dk; ++j) R[(size_t)i * dk + j] = fmaf(-y[i], v[j], R[(size_t)i * dk + j]);
+  }
+  free(V);
+  free(y);
+  free(score);
+  free(taken);
+}
+
+static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st, orc_diag* dg, const float* prev) {
   const int dk = cfg->dk, dv = cfg->dv, L = line_len(cfg);
   float* R = (float*)malloc(sizeof(float) * (size_t)dv * dk);
   float* rho = (float*)malloc(sizeof(float) * dv);
@@ -392,7 +468,9 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
   float* g = (float*)malloc(sizeof(float) * dk);
   memcpy(R, S, sizeof(float) * (size_t)dv * dk);
 
-  if (cfg->comp_fit > 0) {
+  if (cfg->comp_fit > 0 && cfg->comp_block) {
+    fit_block(cfg, R, st, prev);
+  } else if (cfg->comp_fit > 0) {
     fit_factors(cfg, R, st);
   } else {
     /* F2: C greedy rounds. Score of a line = its squared L2 length
@@ -524,7 +602,15 @@ static int fold_one(const orc_cfg* cfg, orc_view st, orc_diag* dg) {
   reconstruct(cfg, st, S);
   if (dg && dg->S) memcpy(dg->S, S, sizeof(float) * (size_t)cfg->dv * cfg->dk);
   if (cfg->quantize) {
-    boundary_from_state(cfg, S, st, dg);
+    /* the block fit starts from this window's factors, read before they are replaced */
+    float* prev = NULL;
+    if (cfg->comp_fit > 0 && cfg->comp_block && cfg->C > 0) {
+      const size_t nb = (size_t)cfg->C * comp_len(cfg);
+      prev = (float*)malloc(sizeof(float) * nb);
+      memcpy(prev, st.comp_line, sizeof(float) * nb);
+    }
+    boundary_from_state(cfg, S, st, dg, prev);
+    free(prev);
   } else {
     memcpy(st.B, S, sizeof(float) * (size_t)cfg->dv * cfg->dk);
     st.count[0] = 0;
@@ -540,6 +626,7 @@ static int cfg_ok(const orc_cfg* c) {
   if (!(c->lambda_floor > 0.0f)) return 0;
   if (c->code_bits < 2 || c->code_bits > 8) return 0;
   if (c->comp_fit < 0 || c->comp_fit > 64) return 0;
+  if (c->comp_block != 0 && c->comp_block != 1) return 0;
   return 1;
 }
 
@@ -557,7 +644,7 @@ int orc_init_state(const orc_cfg* cfg, orc_batch* b, int64_t s, const float* S0,
   }
   if (dg && dg->S) memcpy(dg->S, S0, sizeof(float) * n);
   if (cfg->quantize) {
-    boundary_from_state(cfg, S0, st, dg);
+    boundary_from_state(cfg, S0, st, dg, NULL);
   } else {
     memcpy(st.B, S0, sizeof(float) * n);
     st.count[0] = 0;
@@ -581,6 +668,21 @@ int orc_fold(const orc_cfg* cfg, orc_batch* b, int64_t s, orc_diag* dg) {
 int orc_export(const orc_cfg* cfg, orc_batch* b, int64_t s, float* S_out) {
   if (!cfg_ok(cfg) || s < 0 || s >= b->n_states) return ORC_ERR_ARG;
   reconstruct(cfg, view_of(cfg, b, s), S_out);
+  return ORC_OK;
+}
+
+/* F2 alone, for tests: fit the factors of R [dv][dk] (left deflated in place),
+ * from the previous factors `prev` ([C][dv + dk], or NULL) when comp_block is set. */
+int orc_fit(const orc_cfg* cfg, float* R, const float* prev, float* comp_line, int32_t* comp_id) {
+  if (!cfg_ok(cfg) || cfg->comp_fit <= 0 || !R || !comp_line || !comp_id) return ORC_ERR_ARG;
+  orc_view st;
+  memset(&st, 0, sizeof st);
+  st.comp_line = comp_line;
+  st.comp_id = comp_id;
+  if (cfg->comp_block)
+    fit_block(cfg, R, st, prev);
+  else
+    fit_factors(cfg, R, st);
   return ORC_OK;
 }
 

@@ -31,6 +31,7 @@ class Cfg(ctypes.Structure):
         ("lambda_floor", ctypes.c_float),
         ("code_bits", ctypes.c_int32),
         ("comp_fit", ctypes.c_int32),
+        ("comp_block", ctypes.c_int32),
     ]
 
 
@@ -79,6 +80,8 @@ def lib():
         L.orc_export.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P]
         L.orc_run.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P, _P, _P, _P, _P, _P,
                               ctypes.c_int, ctypes.c_int]
+        L.orc_fit.restype = ctypes.c_int
+        L.orc_fit.argtypes = [ctypes.POINTER(Cfg), _P, _P, _P, _P]
         L.orc_fp32_run.restype = None
         L.orc_fp32_run.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P,
                                    _P, _P, _P, _P, _P, _P]
@@ -120,13 +123,14 @@ class OracleState:
     """Boundary + record buffer for ``n_states`` head-states, as numpy arrays."""
 
     def __init__(self, n_states, dk=128, dv=128, W=16, C=4, decay_per_key=False, smooth=True, quantize=True,
-                 lambda_floor=1e-6, code_bits=8, comp_fit=0):
+                 lambda_floor=1e-6, code_bits=8, comp_fit=0, comp_block=0):
         self.n, self.dk, self.dv, self.W, self.C = int(n_states), int(dk), int(dv), int(W), int(C)
         self.kda = bool(decay_per_key)
         self.code_bits = int(code_bits)
         self.comp_fit = int(comp_fit)
+        self.comp_block = int(comp_block)
         self.cfg = Cfg(self.dk, self.dv, self.W, self.C, int(decay_per_key), int(smooth), int(quantize),
-                       float(lambda_floor), self.code_bits, self.comp_fit)
+                       float(lambda_floor), self.code_bits, self.comp_fit, self.comp_block)
         N, L = self.n, max(self.dk, self.dv)
         alen = self.dk if self.kda else 1
         self.codes = np.zeros((N, self.dv, self.dk), np.int8)
@@ -235,6 +239,23 @@ class OracleState:
             else:
                 B[:, cid - self.dv] += self.comp_line[s, c, :self.dv]
         return B
+
+
+def fit(R, C, sweeps, block=False, prev=None):
+    """F2 alone on R [dv][dk] (fp32): returns (a [C][dv], b [C][dk], ids [C], the deflated
+    residual). block: the block fit, from prev = (a, b) of the previous window when given."""
+    R = _f32(R).copy()
+    dv, dk = R.shape
+    cfg = Cfg(dk, dv, 16, C, 0, 1, 1, 1e-6, 8, int(sweeps), int(bool(block)))
+    out = np.zeros((C, dv + dk), np.float32)
+    ids = np.zeros(C, np.int32)
+    pl = None
+    if prev is not None:
+        pl = np.ascontiguousarray(np.concatenate([_f32(prev[0]), _f32(prev[1])], axis=1))
+    rc = lib().orc_fit(ctypes.byref(cfg), _ptr(R), _ptr(pl), _ptr(out), _ptr(ids))
+    if rc != 0:
+        raise RuntimeError(f"orc_fit failed: {rc}")
+    return out[:, :dv], out[:, dv:], ids, R
 
 
 def fp32_run(S0, q, k, v, alpha, beta, want_o=True):
