@@ -237,13 +237,13 @@ class Pool:
         return [x[t] for x in self.dev]
 
 
-def setup_state(wl, device, state0=0, bits=8, comp_fit=0):
+def setup_state(wl, device, state0=0, bits=8, comp_fit=0, comp_block=0):
     import torch
 
     from quantized_linear_attention_gb300 import lq
     from quantized_linear_attention_gb300 import workload as wlm
 
-    cfg = lq.config(window=wl.W, n_comp=wl.C, kda=wl.kda, code_bits=bits, comp_fit=comp_fit)
+    cfg = lq.config(window=wl.W, n_comp=wl.C, kda=wl.kda, code_bits=bits, comp_fit=comp_fit, comp_block=comp_block)
     S0, _ = wlm.initial_state(wl, state0, wl.n_states)
     state = lq.alloc_state(cfg, wl.n_states, device)
     lq.state_init(cfg, state, wl.n_states, None if S0 is None else torch.from_numpy(S0).to(device))
@@ -251,7 +251,7 @@ def setup_state(wl, device, state0=0, bits=8, comp_fit=0):
     return cfg, state
 
 
-def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0):
+def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0, comp_block=0):
     """The timed region: K windows, a CUDA event between every two launches."""
     import torch
 
@@ -259,7 +259,7 @@ def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0):
 
     W, N = wl.W, wl.n_states
     s0 = shard_offset(wl, rank)
-    cfg, state = setup_state(wl, device, s0, bits, comp_fit)
+    cfg, state = setup_state(wl, device, s0, bits, comp_fit, comp_block)
     pool = Pool(wl, 4 * W, device, state0=s0)
     o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
 
@@ -657,14 +657,17 @@ def run_ours(args):
             "append_gbs": round(b_app_bytes / (b_app_ms / 1e3) / 1e9, 1),
             "append_frac": round(b_app_bytes / (b_app_ms / 1e3) / 1e9 / hbm, 4)}
     if rank == 0 and not args.no_fit:
-        f_total, f_app, f_fold, _ = time_main(wl, args, device, 1, 0, steps=50, comp_fit=8)
-        f_win_ms = f_total / 50
-        result["comp_fit_8"] = {
-            "note": "compensators as rank-one factors fitted by 8 power-iteration sweeps from the longest row "
-                    "(the other reading of Compensator Tokens); 50 timed windows",
-            "head_tokens_per_s": round(N * W / (f_win_ms / 1e3), 1),
-            "append_step_us": round(statistics.mean(f_app) * 1e3, 2),
-            "fold_step_us": round(statistics.mean(f_fold) * 1e3, 2)}
+        for name, sweeps, block, note in (
+                ("comp_fit_8", 8, 0, "compensators as rank-one factors fitted one at a time by 8 power-iteration "
+                                     "sweeps from the longest row (the other reading of Compensator Tokens)"),
+                ("comp_block_4", 4, 1, "the same factors fitted together as a block by 4 sweeps of subspace "
+                                       "iteration, each fold starting from the previous window's factors")):
+            f_total, f_app, f_fold, _ = time_main(wl, args, device, 1, 0, steps=50, comp_fit=sweeps, comp_block=block)
+            result[name] = {
+                "note": note + "; 50 timed windows",
+                "head_tokens_per_s": round(N * W / (f_total / 50 / 1e3), 1),
+                "append_step_us": round(statistics.mean(f_app) * 1e3, 2),
+                "fold_step_us": round(statistics.mean(f_fold) * 1e3, 2)}
     if rank == 0 and not args.no_fp32:
         f_ms = time_fp32(wl, device)
         fb = N * alg_bytes_fp32(wl.kda)

@@ -77,6 +77,9 @@ typedef struct {
                          /* 1..32: a rank-one factor a b^T fitted to the residual by that   */
                          /* many power-iteration sweeps from the longest row ([LQ] §3.3,    */
                          /* App. B.3 "fitting new factors"; [RN4] "Where the time goes")    */
+  int32_t comp_block;    /* with comp_fit > 0: 1 fits the C factors together as a block     */
+                         /* (subspace iteration), each fold starting from the previous      */
+                         /* window's factors ([RN4] "Redesign"); 0 (default) one at a time  */
 } lq_config;
 
 /*

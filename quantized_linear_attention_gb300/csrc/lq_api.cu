@@ -56,6 +56,10 @@ int check_cfg(const lq_config* c) {
     return fail(LQ_ERR_INVALID_ARG, "lambda_floor must be finite and > 0");
   if (c->comp_fit < 0 || c->comp_fit > 32)
     return fail(LQ_ERR_INVALID_ARG, "comp_fit must be 0..32 (got %d)", c->comp_fit);
+  if (c->comp_block != 0 && c->comp_block != 1)
+    return fail(LQ_ERR_INVALID_ARG, "comp_block must be 0 or 1 (got %d)", c->comp_block);
+  if (c->comp_block && c->comp_fit == 0)
+    return fail(LQ_ERR_INVALID_ARG, "comp_block needs fitted factors (comp_fit > 0)");
   if (c->code_bits != 8 && c->code_bits != 6 && c->code_bits != 4) {
     if (c->code_bits >= 2 && c->code_bits <= 7)
       return fail(LQ_ERR_UNSUPPORTED, "code_bits %d: this build runs 8-, 6- and 4-bit codes", c->code_bits);
@@ -70,7 +74,8 @@ int check_n(int64_t n) {
 }
 
 uint64_t cfg_hash(const lq_config* c, int64_t n) {
-  const int64_t f[9] = {c->d_k, c->d_v, c->window, c->n_comp, c->decay_per_key, c->smooth, c->code_bits, c->comp_fit, n};
+  const int64_t f[10] = {c->d_k,       c->d_v,     c->window,   c->n_comp,     c->decay_per_key,
+                         c->smooth,    c->code_bits, c->comp_fit, c->comp_block, n};
   uint32_t fl;
   std::memcpy(&fl, &c->lambda_floor, 4);
   uint64_t h = 1469598103934665603ull;  // FNV-1a
@@ -175,6 +180,7 @@ Params make_params(const lq_config* c, void* state, int64_t n) {
   p.smooth = c->smooth;
   p.bits = c->code_bits;
   p.comp_fit = c->comp_fit;
+  p.comp_block = c->comp_block;
   p.lambda_floor = c->lambda_floor;
   p.phase = -1;
   p.n_states = n;
@@ -243,6 +249,7 @@ void lq_config_default(lq_config* cfg) {
   cfg->smooth = 1;
   cfg->code_bits = 8;
   cfg->comp_fit = 0;
+  cfg->comp_block = 0;
   cfg->lambda_floor = 1e-6f;
 }
 

@@ -49,6 +49,7 @@ struct Params {
   int W, C, kda, smooth;
   int bits;      // code width: 8 or 4
   int comp_fit;  // 0: outlier-line compensators; s > 0: factors fitted by s sweeps
+  int comp_block;  // fitted factors: 1 = block fit from the previous window's factors
   float lambda_floor;
   int phase;  // expected record count before the call, or -1
   int push_full;  // append: list the head-states whose window this token fills

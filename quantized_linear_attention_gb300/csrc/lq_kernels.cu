@@ -1294,8 +1294,11 @@ __device__ __forceinline__ void column_offsets(int j, int coff[8]) {
   for (int k = 0; k < 8; ++k) coff[k] = ((c ^ ((((c >> 3) + k) & 3) | (k & 4))) << 2) + (j & 3);
 }
 
-// Store a thread's rows into the swizzled tile S; record their row partials
-// ([row][block]) and row scores (squared lengths).
+// Store a thread's rows into the swizzled tile S; with SCORES, record their row
+// partials ([row][block]) and row scores (squared lengths) for the line
+// selection (the fits compute their own, and the block fit keeps the previous
+// factors where the partials would go).
+template <bool SCORES>
 __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1304,12 +1307,14 @@ __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float 
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     const int i = 32 * pp + 4 * w + r;
-    float pr = 0.0f;
+    if (SCORES) {
+      float pr = 0.0f;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) pr = __fmaf_rn(acc[pp][t], acc[pp][t], pr);
-    tl.rowpart[i * 8 + qq] = pr;
-    const float rho = tree8(pr);
-    if (qq == 0) tl.score[i] = rho;
+      for (int t = 0; t < 16; ++t) pr = __fmaf_rn(acc[pp][t], acc[pp][t], pr);
+      tl.rowpart[i * 8 + qq] = pr;
+      const float rho = tree8(pr);
+      if (qq == 0) tl.score[i] = rho;
+    }
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4)
       *reinterpret_cast<float4*>(&S[i * kD + roff[c4]]) =
@@ -1519,14 +1524,174 @@ __device__ __forceinline__ void fit_factors_tile(const Params& p, int64_t s, flo
   }
 }
 
+// Canonical dot of two 128-vectors in shared memory, computed by every warp
+// (lane group blocks lane & 7, ascending chains, then the tree).
+__device__ __forceinline__ float fit_dot(const float* a, const float* b) {
+  const int blk = threadIdx.x & 7;
+  float acc = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) acc = __fmaf_rn(a[16 * blk + t], b[16 * blk + t], acc);
+  return tree8(acc);
+}
+
+// Modified Gram-Schmidt over V [C][128] in order: each vector loses its
+// components along the earlier ones (fma per entry), then is normalized
+// through one reciprocal of its length; a zero vector stays zero.
+__device__ __forceinline__ void fit_orthonormalize(float* V, int C) {
+  const int tid = threadIdx.x;
+  for (int c = 0; c < C; ++c) {
+    float* v = V + c * kD;
+    for (int e = 0; e < c; ++e) {
+      const float d = fit_dot(v, V + e * kD);
+      __syncthreads();
+      if (tid < kD) v[tid] = __fmaf_rn(-d, V[e * kD + tid], v[tid]);
+      __syncthreads();
+    }
+    const float inv = fit_inv_norm(v);
+    __syncthreads();
+    if (tid < kD) v[tid] = __fmul_rn(v[tid], inv);
+    __syncthreads();
+  }
+}
+
+// Block fit of the C factors on the tile (subspace iteration): V [C][128] in
+// the tail's row-partial area holds the previous window's unit factors when
+// `warm`; a zero (or absent) one starts from the c-th longest row instead.
+// Sweeps of {orthonormalize V; v_c = R^T (R v_c)}, a last orthonormalization,
+// then per factor a_c = R v_c, stored with v_c, and the deflation.
+__device__ __forceinline__ void fit_block_tile(const Params& p, int64_t s, float* S, const Tail& tl, bool warm) {
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float* V = tl.rowpart;
+  float* y = tl.score2;
+  int roff[4];
+  row_offsets(4 * w + r, qq, roff);
+  const int cb = tid >> 5, cq = tid & 31;  // column walks: rows 16cb.., columns 4cq..4cq+3
+  int coff[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) coff[k] = (cq ^ ((((cq >> 3) + k) & 3) | (k & 4))) << 2;
+  __shared__ int s_rows[kMaxC];
+  const int C = p.C;
+  // the C longest rows, in order (squared length, ties to the smaller row)
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
+    float acc = 0.0f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 x = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
+      acc = __fmaf_rn(x.x, x.x, acc);
+      acc = __fmaf_rn(x.y, x.y, acc);
+      acc = __fmaf_rn(x.z, x.z, acc);
+      acc = __fmaf_rn(x.w, x.w, acc);
+    }
+    acc = tree8(acc);
+    if (qq == 0) tl.score[i] = acc;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int L = tid & 31;
+    float sc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[e] = tl.score[L + 32 * e];
+    for (int c = 0; c < C; ++c) {
+      float bsc = sc[0];
+      int bi = L;
+#pragma unroll
+      for (int e = 1; e < 4; ++e) {
+        if (sc[e] > bsc) {
+          bsc = sc[e];
+          bi = L + 32 * e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bsc || (ov == bsc && oi < bi)) {
+          bsc = ov;
+          bi = oi;
+        }
+      }
+      if (L == 0) s_rows[c] = bi;
+      if ((bi & 31) == L) sc[bi >> 5] = -1.0f;  // taken (scores are >= 0)
+    }
+  }
+  __syncthreads();
+  for (int c = 0; c < C; ++c) {
+    const bool keep = warm && __syncthreads_or(tid < kD && V[c * kD + (tid & (kD - 1))] != 0.0f);
+    if (!keep && tid < kD) V[c * kD + tid] = S[sidx(s_rows[c], tid)];
+  }
+  __syncthreads();
+  for (int sw = 0; sw < p.comp_fit; ++sw) {
+    fit_orthonormalize(V, C);
+    for (int c = 0; c < C; ++c) {
+      fit_row_walk(S, V + c * kD, 1.0f, y, roff);
+      __syncthreads();
+      float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+      const float* base = S + 16 * cb * kD;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float ai = y[16 * cb + t];
+        const float4 x = *reinterpret_cast<const float4*>(base + t * kD + coff[t & 7]);
+        c0 = __fmaf_rn(x.x, ai, c0);
+        c1 = __fmaf_rn(x.y, ai, c1);
+        c2 = __fmaf_rn(x.z, ai, c2);
+        c3 = __fmaf_rn(x.w, ai, c3);
+      }
+      *reinterpret_cast<float4*>(tl.colpart + cb * kD + 4 * cq) = make_float4(c0, c1, c2, c3);
+      __syncthreads();
+      if (tid < kD) V[c * kD + tid] = tree8_mem(tl.colpart + tid, kD);
+      __syncthreads();
+    }
+  }
+  fit_orthonormalize(V, C);
+  for (int c = 0; c < C; ++c) {
+    const float* v = V + c * kD;
+    fit_row_walk(S, v, 1.0f, y, roff);
+    __syncthreads();
+    float* out = p.comp_line + (s * p.C + c) * (2 * kD);
+    if (tid < kD) {
+      out[tid] = y[tid];
+      out[kD + tid] = v[tid];
+    }
+    if (tid == 0) p.comp_id[s * p.comp_id_stride + c] = c;
+    float bq[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) bq[t] = v[16 * qq + t];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = 32 * pp + 4 * w + r;
+      const float na = -y[i];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float4* e = reinterpret_cast<float4*>(&S[i * kD + roff[c4]]);
+        float4 x = *e;
+        x.x = __fmaf_rn(na, bq[4 * c4 + 0], x.x);
+        x.y = __fmaf_rn(na, bq[4 * c4 + 1], x.y);
+        x.z = __fmaf_rn(na, bq[4 * c4 + 2], x.z);
+        x.w = __fmaf_rn(na, bq[4 * c4 + 3], x.w);
+        *e = x;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // F2-F6 on the state tile S, with row partials and row scores in the tail.
+// `warm`: the tail's row-partial area holds the previous window's factors
+// (fitted factors in block form).
 template <int BITS, bool FIT>
-__device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl) {
+__device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, float* S, const Tail& tl,
+                                                   bool warm = false) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
 
   if (FIT) {
-    fit_factors_tile(p, s, S, tl);
+    if (p.comp_block)
+      fit_block_tile(p, s, S, tl, warm);
+    else
+      fit_factors_tile(p, s, S, tl);
   } else {
   int coff[8];
   column_offsets(tid & (kD - 1), coff);
@@ -1756,6 +1921,18 @@ namespace lqi {
 
 extern __shared__ __align__(128) char lq_dyn_smem[];
 
+// Block fit: the previous window's unit factors b_c (staged with the
+// compensator lines) go to the tail before the tile overwrites the staging.
+template <bool FIT>
+__device__ __forceinline__ void keep_factors(const Params& p, const Tail& tl) {
+  if (FIT && p.comp_block) {
+    const float* cl = at<float>(lq_dyn_smem, p.st.comp_line);
+    for (int e = threadIdx.x; e < p.C * kD; e += blockDim.x)
+      tl.rowpart[e] = cl[(2 * (e / kD) + 1) * kD + (e & (kD - 1))];
+  }
+}
+
+
 // Thread 0 starts the copies (at once when `known_n0` >= 0, else after reading
 // the record count), checks the header and publishes what it found in shared
 // memory; returns after the __syncthreads that makes it visible.
@@ -1933,11 +2110,12 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
   reconstruct_rows<KDA, BITS, FIT>(p, n, L, lq_dyn_smem, acc);
-  __syncthreads();  // every staged input has been read: the tile may overwrite them
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
+  keep_factors<FIT>(p, tl);
+  __syncthreads();  // every staged input has been read: the tile may overwrite them
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows(S, tl, acc);
-  boundary_from_tile<BITS, FIT>(p, s, S, tl);
+  tile_store_rows<!FIT>(S, tl, acc);
+  boundary_from_tile<BITS, FIT>(p, s, S, tl, true);
 }
 
 // F0-F6 on a staged head-state holding n records.
@@ -1950,11 +2128,12 @@ __device__ __forceinline__ void fold_staged(const Params& p, int64_t s, int n) {
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
   reconstruct_rows<KDA, BITS, FIT>(p, n, L, lq_dyn_smem, acc);
-  __syncthreads();
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
+  keep_factors<FIT>(p, tl);
+  __syncthreads();
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows(S, tl, acc);
-  boundary_from_tile<BITS, FIT>(p, s, S, tl);
+  tile_store_rows<!FIT>(S, tl, acc);
+  boundary_from_tile<BITS, FIT>(p, s, S, tl, true);
 }
 
 // Fold with the records held (any count 0..W): lq_fold.
@@ -2089,7 +2268,7 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
   }
   const Tail tl = carve_tail(lq_dyn_smem, p.r1);
   float* S = reinterpret_cast<float*>(lq_dyn_smem);
-  tile_store_rows(S, tl, acc);
+  tile_store_rows<!FIT>(S, tl, acc);
   boundary_from_tile<BITS, FIT>(p, s, S, tl);
 }
 

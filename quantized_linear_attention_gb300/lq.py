@@ -36,7 +36,8 @@ EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", 
 class Config(ctypes.Structure):
     _fields_ = [("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("n_comp", ctypes.c_int32), ("decay_per_key", ctypes.c_int32), ("smooth", ctypes.c_int32),
-                ("lambda_floor", ctypes.c_float), ("code_bits", ctypes.c_int32), ("comp_fit", ctypes.c_int32)]
+                ("lambda_floor", ctypes.c_float), ("code_bits", ctypes.c_int32), ("comp_fit", ctypes.c_int32),
+                ("comp_block", ctypes.c_int32)]
 
 
 class Layout(ctypes.Structure):
@@ -107,8 +108,9 @@ def _check(rc):
 
 
 def config(window=16, n_comp=4, kda=False, smooth=True, lambda_floor=1e-6, d_k=128, d_v=128, code_bits=8,
-           comp_fit=0) -> Config:
-    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor, code_bits, comp_fit)
+           comp_fit=0, comp_block=0) -> Config:
+    return Config(d_k, d_v, window, n_comp, int(bool(kda)), int(bool(smooth)), lambda_floor, code_bits, comp_fit,
+                  int(comp_block))
 
 
 def default_config() -> Config:

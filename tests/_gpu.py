@@ -43,10 +43,11 @@ def unpack_codes(codes):
 
 
 class GpuState:
-    def __init__(self, n, W=16, C=4, kda=False, smooth=True, lambda_floor=1e-6, code_bits=8, comp_fit=0):
+    def __init__(self, n, W=16, C=4, kda=False, smooth=True, lambda_floor=1e-6, code_bits=8, comp_fit=0,
+                 comp_block=0):
         self.n, self.W, self.C, self.kda = n, W, C, kda
         self.cfg = lq.config(window=W, n_comp=C, kda=kda, smooth=smooth, lambda_floor=lambda_floor,
-                             code_bits=code_bits, comp_fit=comp_fit)
+                             code_bits=code_bits, comp_fit=comp_fit, comp_block=comp_block)
         self.state = lq.alloc_state(self.cfg, n, DEV)
         self.views = lq.state_views(self.cfg, self.state, n)
         self.o = torch.empty((n, 128), dtype=torch.float32, device=DEV)
@@ -121,7 +122,7 @@ def compare_boundary(g, ref: OracleState, ref_idx, diags=None, tally: Tally | No
 
 
 def run_and_compare(wl: wlm.Workload, n_tokens: int, sample=None, phase_mode="stated", chunk=64, W=None, C=None,
-                    smooth=True, tally=None, use_append_fold=False, code_bits=8, comp_fit=0):
+                    smooth=True, tally=None, use_append_fold=False, code_bits=8, comp_fit=0, comp_block=0):
     """Free-running decode of n_tokens for all wl.n_states head-states on the GPU; the
     oracle follows the sampled states. Compares o every token, records every
     token, boundaries after every fold. Returns the Tally."""
@@ -131,10 +132,11 @@ def run_and_compare(wl: wlm.Workload, n_tokens: int, sample=None, phase_mode="st
     sample = list(range(N)) if sample is None else list(sample)
     tally = tally or Tally()
     S0, _ = wlm.initial_state(wl)
-    gpu = GpuState(N, W=W, C=C, kda=wl.kda, smooth=smooth, code_bits=code_bits, comp_fit=comp_fit)
+    gpu = GpuState(N, W=W, C=C, kda=wl.kda, smooth=smooth, code_bits=code_bits, comp_fit=comp_fit,
+                   comp_block=comp_block)
     gpu.init(S0)
     ref = OracleState(len(sample), W=W, C=C, decay_per_key=wl.kda, smooth=smooth, code_bits=code_bits,
-                      comp_fit=comp_fit)
+                      comp_fit=comp_fit, comp_block=comp_block)
     d0 = [FoldDiag(128, 128) for _ in sample]
     ref.init(None if S0 is None else S0[sample], diags=d0)
     sidx = torch.as_tensor(sample, device=DEV)

@@ -112,7 +112,8 @@ def test_layout_planes(L, n, kda):
     ("lambda_floor", 0.0, lq.ERR_INVALID_ARG), ("lambda_floor", float("inf"), lq.ERR_INVALID_ARG),
     ("code_bits", 5, lq.ERR_UNSUPPORTED), ("code_bits", 7, lq.ERR_UNSUPPORTED), ("code_bits", 9, lq.ERR_INVALID_ARG),
     ("code_bits", 0, lq.ERR_INVALID_ARG),
-    ("comp_fit", -1, lq.ERR_INVALID_ARG), ("comp_fit", 33, lq.ERR_INVALID_ARG)])
+    ("comp_fit", -1, lq.ERR_INVALID_ARG), ("comp_fit", 33, lq.ERR_INVALID_ARG),
+    ("comp_block", 1, lq.ERR_INVALID_ARG), ("comp_block", 2, lq.ERR_INVALID_ARG)])
 def test_invalid_config_rejected(L, field, value, code):
     cfg = lq.default_config()
     setattr(cfg, field, value)
@@ -120,6 +121,12 @@ def test_invalid_config_rejected(L, field, value, code):
     rc = L.lq_layout(ctypes.byref(cfg), 4, ctypes.byref(lq.Layout()))
     assert rc == code
     assert lq.last_error() != ""
+
+
+def test_block_fit_needs_fitted_factors_and_changes_the_header_hash(L):
+    ok = lq.config(comp_fit=2, comp_block=1)
+    assert L.lq_layout(ctypes.byref(ok), 4, ctypes.byref(lq.Layout())) == lq.OK
+    assert lq.layout(ok, 4).total_bytes == lq.layout(lq.config(comp_fit=2), 4).total_bytes
 
 
 def test_invalid_sizes_and_nulls_rejected_on_host(L):
