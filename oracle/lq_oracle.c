@@ -653,6 +653,128 @@ int orc_init_state(const orc_cfg* cfg, orc_batch* b, int64_t s, const float* S0,
   return ORC_OK;
 }
 
+/*
+ * S_h x for a state holding h records and an explicit read vector x: the read
+ * of the state as it stands, before any decay of the token being added
+ * ([LQ] App. B.2 window unrolling with the decay products of the held records
+ * only; App. B.3 smoothing on the residual term): P_h = 1,
+ * P_{m-1} = P_m . alpha_m; y = P_0 . x, z = lambda . y;
+ *   acc_i = sigma_i dot(codes_i, z), then fma(a_c[i], dot(b_c, y), .) for each
+ *   compensator, then fma(u_m[i], dot(k_m, P_m . x), .) for m = 1..h.
+ */
+static void read_at(const orc_cfg* cfg, orc_view st, const float* x, float* acc) {
+  const int dk = cfg->dk, dv = cfg->dv, alen = alpha_len(cfg);
+  const int h = st.count[0];
+  float* P = (float*)malloc(sizeof(float) * (size_t)(h + 1) * alen);
+  float* y = (float*)malloc(sizeof(float) * dk);
+  float* z = (float*)malloc(sizeof(float) * dk);
+  float* xm = (float*)malloc(sizeof(float) * dk);
+  float* row = (float*)malloc(sizeof(float) * dk);
+  float* ca = (float*)malloc(sizeof(float) * dv);
+  float* cb = (float*)malloc(sizeof(float) * dk);
+  decay_products(h, alen, st.rec_alpha, P);
+  for (int j = 0; j < dk; ++j) y[j] = pj(P, alen, j) * x[j];
+  if (cfg->quantize)
+    for (int j = 0; j < dk; ++j) z[j] = st.lambda[j] * y[j];
+  for (int i = 0; i < dv; ++i) {
+    if (cfg->quantize) {
+      for (int j = 0; j < dk; ++j) row[j] = (float)st.codes[(size_t)i * dk + j];
+      acc[i] = st.sigma[i] * orc_dot(dk, row, 1, z, 1);
+    } else {
+      acc[i] = orc_dot(dk, st.B + (size_t)i * dk, 1, y, 1);
+    }
+  }
+  for (int c = 0; c < cfg->C; ++c) {
+    comp_vectors(cfg, st, c, ca, cb);
+    const float e = orc_dot(dk, cb, 1, y, 1);
+    for (int i = 0; i < dv; ++i) acc[i] = fmaf(ca[i], e, acc[i]);
+  }
+  for (int m = 1; m <= h; ++m) {
+    const float* Pm = P + (size_t)m * alen;
+    for (int j = 0; j < dk; ++j) xm[j] = pj(Pm, alen, j) * x[j];
+    const float g = orc_dot(dk, st.rec_k + (size_t)(m - 1) * dk, 1, xm, 1);
+    const float* um = st.rec_u + (size_t)(m - 1) * dv;
+    for (int i = 0; i < dv; ++i) acc[i] = fmaf(um[i], g, acc[i]);
+  }
+  free(P);
+  free(y);
+  free(z);
+  free(xm);
+  free(row);
+  free(ca);
+  free(cb);
+}
+
+/* o = S_h q in double for a state holding h records (the output; its order is
+ * not part of the state and it is compared with a tolerance). */
+static void output_of(const orc_cfg* cfg, orc_view st, const float* q, double* o) {
+  const int dk = cfg->dk, dv = cfg->dv, alen = alpha_len(cfg);
+  const int h = st.count[0];
+  float* P = (float*)malloc(sizeof(float) * (size_t)(h + 1) * alen);
+  float* ca = (float*)malloc(sizeof(float) * dv);
+  float* cb = (float*)malloc(sizeof(float) * dk);
+  double* w = (double*)malloc(sizeof(double) * dk);
+  decay_products(h, alen, st.rec_alpha, P);
+  for (int j = 0; j < dk; ++j) w[j] = (double)pj(P, alen, j) * (double)q[j];
+  for (int i = 0; i < dv; ++i) {
+    double sum = 0.0;
+    for (int j = 0; j < dk; ++j)
+      sum += (cfg->quantize ? (double)st.sigma[i] * (double)st.codes[(size_t)i * dk + j] * (double)st.lambda[j]
+                            : (double)st.B[(size_t)i * dk + j]) *
+             w[j];
+    o[i] = sum;
+  }
+  for (int c = 0; c < cfg->C; ++c) {
+    comp_vectors(cfg, st, c, ca, cb);
+    double e = 0.0;
+    for (int j = 0; j < dk; ++j) e += (double)cb[j] * w[j];
+    for (int i = 0; i < dv; ++i) o[i] += (double)ca[i] * e;
+  }
+  for (int m = 1; m <= h; ++m) {
+    const float* Pm = P + (size_t)m * alen;
+    double hh = 0.0;
+    for (int j = 0; j < dk; ++j)
+      hh += (double)st.rec_k[(size_t)(m - 1) * dk + j] * (double)pj(Pm, alen, j) * (double)q[j];
+    for (int i = 0; i < dv; ++i) o[i] += (double)st.rec_u[(size_t)(m - 1) * dv + i] * hh;
+  }
+  free(P);
+  free(ca);
+  free(cb);
+  free(w);
+}
+
+/*
+ * One RWKV7 token as two records ([LQ] App. A: a token whose erase direction
+ * differs from its write key is split into an erase and a pure-write sub-step,
+ * two rank-one records). With S_t = S_{t-1} (Diag(w) - kh (a . kh)^T) + v k^T
+ * and o = S_t r:
+ *   record n   = (a . kh, u_e, w),  u_e = -(S_{n-1} kh)  (the read before decay);
+ *   record n+1 = (k, v, 1)           (no read);
+ *   o = S_{n+1} r.
+ * Per-key decay only (decay_per_key = 1).
+ */
+int orc_append_rwkv(const orc_cfg* cfg, orc_batch* b, int64_t s, const float* r, const float* w, const float* kh,
+                    const float* a, const float* k, const float* v, double* o) {
+  if (!cfg_ok(cfg) || s < 0 || s >= b->n_states || !cfg->decay_per_key) return ORC_ERR_ARG;
+  orc_view st = view_of(cfg, b, s);
+  const int dk = cfg->dk, dv = cfg->dv;
+  const int h = st.count[0];
+  if (h + 2 > cfg->W) return ORC_ERR_WINDOW_FULL;
+  float* acc = (float*)malloc(sizeof(float) * dv);
+  read_at(cfg, st, kh, acc);
+  float* e_key = st.rec_k + (size_t)h * dk;
+  for (int j = 0; j < dk; ++j) e_key[j] = a[j] * kh[j];
+  for (int i = 0; i < dv; ++i) st.rec_u[(size_t)h * dv + i] = -acc[i];
+  memcpy(st.rec_alpha + (size_t)h * dk, w, sizeof(float) * dk);
+  memcpy(st.rec_k + (size_t)(h + 1) * dk, k, sizeof(float) * dk);
+  memcpy(st.rec_u + (size_t)(h + 1) * dv, v, sizeof(float) * dv);
+  for (int j = 0; j < dk; ++j) st.rec_alpha[(size_t)(h + 1) * dk + j] = 1.0f;
+  st.count[0] = h + 2;
+  if (o) output_of(cfg, st, r, o);
+  free(acc);
+  return ORC_OK;
+}
+
 int orc_append(const orc_cfg* cfg, orc_batch* b, int64_t s, const float* q, const float* k, const float* v,
                const float* alpha, float beta, double* o) {
   if (!cfg_ok(cfg) || s < 0 || s >= b->n_states) return ORC_ERR_ARG;

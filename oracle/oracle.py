@@ -80,6 +80,9 @@ def lib():
         L.orc_export.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P]
         L.orc_run.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P, _P, _P, _P, _P, _P,
                               ctypes.c_int, ctypes.c_int]
+        L.orc_append_rwkv.restype = ctypes.c_int
+        L.orc_append_rwkv.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Batch), ctypes.c_int64, _P, _P, _P, _P, _P,
+                                      _P, _P]
         L.orc_fit.restype = ctypes.c_int
         L.orc_fit.argtypes = [ctypes.POINTER(Cfg), _P, _P, _P, _P]
         L.orc_fp32_run.restype = None
@@ -214,6 +217,19 @@ class OracleState:
                            _ptr(alpha), _ptr(beta), _ptr(o), int(bool(fold_when_full)), int(nthreads))
         if rc != 0:
             raise RuntimeError(f"orc_run failed: {rc}")
+        return o
+
+    def append_rwkv(self, r, w, kh, a, k, v):
+        """One RWKV7 token (erase record, then pure-write record) into every state:
+        r, w, kh, a, k [N][dk], v [N][dv]. Returns o [N][dv] (float64)."""
+        r, w, kh, a, k, v = (_f32(x) for x in (r, w, kh, a, k, v))
+        o = np.zeros((self.n, self.dv), np.float64)
+        L = lib()
+        for s in range(self.n):
+            rc = L.orc_append_rwkv(ctypes.byref(self.cfg), ctypes.byref(self.batch), s, _ptr(r[s]), _ptr(w[s]),
+                                   _ptr(kh[s]), _ptr(a[s]), _ptr(k[s]), _ptr(v[s]), _ptr(o[s]))
+            if rc != 0:
+                raise RuntimeError(f"orc_append_rwkv failed: {rc}")
         return o
 
     # -- views -------------------------------------------------------------
