@@ -390,6 +390,52 @@ def time_two_record(wl, device, steps=50, warmup=3):
     return ev[0].elapsed_time(ev[-1]), app, fold
 
 
+def time_rwkv(device, steps=50, warmup=3):
+    """RWKV7 tokens at batch 512 (16,384 head-states, per-key decay): W/2
+    lq_decode_step_rwkv7 calls per window at stated phases; the last also folds.
+    Token t takes decay and erase direction from generator token 2t, the rest
+    from token 2t+1 (the erase direction normalized)."""
+    import torch
+
+    from quantized_linear_attention_gb300 import lq
+    from quantized_linear_attention_gb300 import workload as wlm
+
+    wl = wlm.custom(4000, 16384, 0, kda=True, n_warm=64, plant=True)
+    W, N = wl.W, wl.n_states
+    per_win = W // 2
+    cfg, state = setup_state(wl, device)
+    pool = Pool(wl, 4 * W, device)
+    kh_pool = [torch.nn.functional.normalize(pool.token(2 * t)[1], dim=-1) for t in range(2 * W)]
+    o = torch.empty((N, wl.dv), dtype=torch.float32, device=device)
+
+    def launch(t):
+        _, _, _, w, _ = pool.token(2 * t)
+        r, k, v, a, _ = pool.token(2 * t + 1)
+        lq.decode_step_rwkv7(cfg, state, N, r, w, kh_pool[t % (2 * W)], a, k, v, o, phase=(2 * t) % W)
+
+    tok = 0
+    for _ in range(warmup * per_win):
+        launch(tok)
+        tok += 1
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * per_win + 1)]
+    ev[0].record()
+    for i in range(steps * per_win):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    status, bad = lq.get_status(state)
+    if status != lq.OK:
+        raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * per_win)]
+    app = [d[i] for i in range(len(d)) if i % per_win != per_win - 1]
+    fold = [d[i] for i in range(len(d)) if i % per_win == per_win - 1]
+    del state, pool
+    torch.cuda.empty_cache()
+    return ev[0].elapsed_time(ev[-1]), app, fold
+
+
 def time_graphed(wl, steps, device):
     """Small batches are launch-bound: capture the W-1 appends and the fold step as
     two CUDA graphs per pool window and time their replays."""
@@ -641,6 +687,17 @@ def run_ours(args):
             "append2_us": round(1e3 * statistics.mean(t_app), 2),
             "fold_token_us": round(1e3 * statistics.mean(t_fold), 2),
             "two_one_record_steps_us": round(2e3 * t_ms / K / W, 2)}
+    if rank == 0 and not args.no_two:
+        r_total, r_app, r_fold = time_rwkv(device)
+        n_tok = len(r_app) + len(r_fold)
+        result["rwkv7"] = {
+            "note": "RWKV7 tokens (lq_decode_step_rwkv7: an erase record and a pure-write record, one kernel per "
+                    f"token) on {N} head-states with per-key decay; {W // 2} tokens per {W}-record window, the "
+                    "last one adds the list fold; 50 timed windows",
+            "head_tokens_per_s": round(N * n_tok / (r_total / 1e3), 1),
+            "token_us_mean": round(1e3 * r_total / n_tok, 2),
+            "append_us": round(1e3 * statistics.mean(r_app), 2),
+            "fold_token_us": round(1e3 * statistics.mean(r_fold), 2)}
     for bits in (6, 4):
         if rank != 0 or args.no_bits4:
             break
@@ -761,7 +818,7 @@ def main(argv=None):
     ap.add_argument("--no-bits4", action="store_true", help="skip the 6- and 4-bit-code runs of the same workload")
     ap.add_argument("--no-fit", action="store_true", help="skip the fitted-factor compensator run")
     ap.add_argument("--no-stagger", action="store_true", help="skip the mixed-window-phase run")
-    ap.add_argument("--no-two", action="store_true", help="skip the two-record-token run")
+    ap.add_argument("--no-two", action="store_true", help="skip the two-record-token and RWKV7 runs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

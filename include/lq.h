@@ -211,6 +211,23 @@ int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t
                     const float* beta2, const float* alpha, float* o, lq_stream_t stream);
 
 /*
+ * One RWKV7 token for every head-state (per-key decay: cfg->decay_per_key = 1).
+ * RWKV7's erase direction differs from its write key, so LeapQuant App. A
+ * ("Instances of the general update") splits the token into an erase and a
+ * pure-write sub-step, two records:
+ *   S_t = S_{t-1} (Diag(w) - kh (a . kh)^T) + v k^T,   o = S_t r;
+ *   record n   = (a . kh, -(S_{n-1} kh), w)   the erase reads the state as it stands;
+ *   record n+1 = (k, v, 1)                     the pure write reads nothing.
+ * kh is the (normalized) erase direction, a its per-key rate, w the per-key decay.
+ * Phases, folding and errors as lq_decode_step2 (two records per token; phase
+ * 0..W-2 or LQ_PHASE_ANY); LQ_ERR_UNSUPPORTED for scalar decay or W < 2.
+ *   r, w, kh, a, k fp32 [n_states][d_k];  v, o fp32 [n_states][d_v]
+ */
+int lq_decode_step_rwkv7(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* r,
+                         const float* w, const float* kh, const float* a, const float* k, const float* v, float* o,
+                         lq_stream_t stream);
+
+/*
  * Write the state each head-state stands for, S_n = boundary x Diag(A_n) plus
  * the buffered records, in original coordinates (the fold's reconstruction,
  * without rounding), to S_out fp32 [n_states][d_v][d_k]. The state is unchanged.

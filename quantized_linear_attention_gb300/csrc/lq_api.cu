@@ -390,6 +390,40 @@ int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t
   return launched(e, "lq_decode_step2 launch");
 }
 
+int lq_decode_step_rwkv7(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* r,
+                         const float* w, const float* kh, const float* a, const float* k, const float* v, float* o,
+                         lq_stream_t stream) {
+  int dev = 0;
+  int rc = check_common(cfg, state, n_states, stream, &dev);
+  if (rc) return rc;
+  if (!cfg->decay_per_key) return fail(LQ_ERR_UNSUPPORTED, "RWKV7 tokens need per-key decay (decay_per_key = 1)");
+  if (cfg->window < 2) return fail(LQ_ERR_UNSUPPORTED, "two-record tokens need a window of at least 2 records");
+  if (phase != LQ_PHASE_ANY && (phase < 0 || phase > cfg->window - 2))
+    return fail(LQ_ERR_INVALID_ARG, "phase must be LQ_PHASE_ANY or 0..W-2 (got %d)", phase);
+  if (n_states == 0) return ok();
+  const void* in[6] = {r, w, kh, a, k, v};
+  const char* names[6] = {"r", "w", "kh", "a", "k", "v"};
+  for (int t = 0; t < 6; ++t)
+    if ((rc = check_ptr(in[t], names[t], 16, dev))) return rc;
+  if ((rc = check_ptr(o, "o", 16, dev))) return rc;
+  const size_t vec = (size_t)n_states * kD * sizeof(float);
+  for (int t = 0; t < 6; ++t)
+    if (overlaps(o, vec, in[t], vec)) return fail(LQ_ERR_INVALID_ARG, "o overlaps an input");
+  Params p = make_params(cfg, state, n_states);
+  p.q = r;
+  p.alpha = w;
+  p.kh = kh;
+  p.ka = a;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.phase = phase;
+  p.push_full = (phase == LQ_PHASE_ANY || phase == cfg->window - 2) ? 1 : 0;
+  cudaError_t e = lqi::launch_append_rwkv(p, (cudaStream_t)stream);
+  if (e == cudaSuccess && p.push_full) e = lqi::launch_fold_listed(p, (cudaStream_t)stream);
+  return launched(e, "lq_decode_step_rwkv7 launch");
+}
+
 int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, float* S_out, lq_stream_t stream) {
   int dev = 0;
   int rc = check_common(cfg, state, n_states, stream, &dev);

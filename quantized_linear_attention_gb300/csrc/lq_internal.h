@@ -41,6 +41,8 @@ struct Stage {
   int basek, baseq, P, g, h, ec, eq;
   // two-record tokens: the second record's key, read vector and sums
   int k2n_b, zk2_b, basek2, g2, ec2;
+  // RWKV7 tokens: the erase key and the decay products of the held records
+  int en_b, Pp_b;
   int end;
 };
 
@@ -76,6 +78,8 @@ struct Params {
   const float* k2;  // two-record tokens: the second record's key, value and step
   const float* v2;
   const float* beta2;
+  const float* kh;  // RWKV7 tokens: the erase direction and its per-key rate
+  const float* ka;
   float* o;
   const float* S0;  // init source (NULL: zero)
   float* S_out;     // export target
@@ -99,6 +103,7 @@ struct Fp32Params {
 cudaError_t launch_init(const Params& p, cudaStream_t st);
 cudaError_t launch_append(const Params& p, cudaStream_t st);
 cudaError_t launch_append2(const Params& p, cudaStream_t st);
+cudaError_t launch_append_rwkv(const Params& p, cudaStream_t st);
 cudaError_t launch_step(const Params& p, cudaStream_t st);
 cudaError_t launch_fold(const Params& p, cudaStream_t st);
 cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st);

@@ -300,7 +300,8 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 // when the keys travel in registers). The token's q, k, v (and alpha) are read
 // into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
-                                              bool append, bool fold, int bits, int comp_fit, bool two = false) {
+                                              bool append, bool fold, int bits, int comp_fit, bool two = false,
+                                              bool rwkv = false) {
   Stage L;
   int o = 0;
   auto take = [&](int bytes) {
@@ -338,6 +339,9 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.basek2 = take(tw * 4 * kD);
   L.g2 = take(tw * 4 * (W + 1));
   L.ec2 = take(tw * 4 * (C > 0 ? C : 1));
+  const int rw = rwkv ? 1 : 0;
+  L.en_b = take(rw * 4 * kBV);
+  L.Pp_b = take(rw * kda * 4 * kBV * W);
   L.end = o;
   return L;
 }
@@ -774,6 +778,246 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       ru[(n - 1) * kD + i] = u;
       at<float>(sm, L.rec_k)[(n - 1) * kD + i] = tk.k;
     }
+  }
+}
+
+// RWKV7 token (per-key decay): with S_t = S_{t-1} (Diag(w) - kh (a . kh)^T) +
+// v k^T and o = S_t r, records n = (a . kh, u_e, w) and n+1 = (k, v, 1) of a
+// head-state holding n-1 records (LeapQuant App. A: an erase and a pure-write
+// sub-step). u_e = -(S_{n-1} kh) reads the state as it stands: the decay
+// products of the held records only (P', P'_{n-1} = 1), so the read does not
+// carry this token's decay; the output uses the products of the state after
+// record n (P, P_n = 1, P_{n-1} = w). One pass over the codes gives the read
+// and the output (two chains per code). 128 threads.
+template <int BITS, bool FIT>
+__device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
+                                                    const TokenRegs& tk, float khv, float kav,
+                                                    const float4 (&kpre)[4]) {
+  constexpr int NW = 4, RPT = 8, NG = 16;
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+  float* P_b = at<float>(sm, L.P_b);
+  float* Pp_b = at<float>(sm, L.Pp_b);
+  float* kn_b = at<float>(sm, L.kn_b);    // write key k
+  float* khn_b = at<float>(sm, L.k2n_b);  // erase direction kh
+  float* en_b = at<float>(sm, L.en_b);    // erase key a . kh
+  float* qn_b = at<float>(sm, L.qn_b);    // r
+  float* zk_b = at<float>(sm, L.zk_b);    // lambda . (P'_0 . kh)
+  float* zq_b = at<float>(sm, L.zq_b);    // lambda . (P_0 . r)
+  float* basek = at<float>(sm, L.basek);
+  float* baseq = at<float>(sm, L.baseq);
+  float* g = at<float>(sm, L.g);
+  float* h = at<float>(sm, L.h);
+  float* ec = at<float>(sm, L.ec);
+  float* eq = at<float>(sm, L.eq);
+  const float* ra = at<float>(sm, L.rec_alpha);
+  const float* sg = at<float>(sm, L.sigma);
+  const float* lam = at<float>(sm, L.lambda);
+  const int32_t* cid = at<int32_t>(sm, L.comp_id);
+  const float* cl = at<float>(sm, L.comp_line);
+
+  // A0: both product chains of column j.
+  if (tid < kD) {
+    const int jb = bv(tid);
+    float pr = 1.0f;
+    P_b[n * kBV + jb] = pr;
+    pr = __fmul_rn(pr, tk.a);
+    P_b[(n - 1) * kBV + jb] = pr;
+    float pp = 1.0f;
+    Pp_b[(n - 1) * kBV + jb] = pp;
+    for (int m = n - 1; m >= 1; --m) {
+      const float am = ra[(m - 1) * kD + tid];
+      pr = __fmul_rn(pr, am);
+      P_b[(m - 1) * kBV + jb] = pr;
+      pp = __fmul_rn(pp, am);
+      Pp_b[(m - 1) * kBV + jb] = pp;
+    }
+  }
+  __syncthreads();
+  // A1: the blocked vectors and the read and output vectors.
+  if (tid < kD) {
+    const int j = tid, jb = bv(j);
+    kn_b[jb] = tk.k;
+    khn_b[jb] = khv;
+    en_b[jb] = __fmul_rn(kav, khv);
+    qn_b[jb] = tk.q;
+    zk_b[jb] = __fmul_rn(lam[j], __fmul_rn(Pp_b[jb], khv));
+    zq_b[jb] = __fmul_rn(lam[j], __fmul_rn(P_b[jb], tk.q));
+  }
+  __syncthreads();
+
+  // Dot products, one lane group each: records m = 1..n-1 against kh (read,
+  // with P'_m) and r (output, with P_m); the compensators against both; the
+  // erase key against r (P_n = 1); k . r.
+  {
+    const int grp = tid >> 3;
+    const int nrec = n - 1;
+    const int njobs = nrec + p.C + 2;
+    for (int base = 0; base < njobs; base += NG) {
+      const int job = base + grp;
+      float pa = 0.0f, pb = 0.0f;
+      if (job < njobs) {
+        const float4* kh4 = reinterpret_cast<const float4*>(khn_b + 20 * qq);
+        const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
+        if (job < nrec) {
+          float4 kv[4];
+          if (base == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = kpre[c4];
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * p.W + job) * kD + 16 * qq);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) kv[c4] = src[c4];
+          }
+          const int m = job + 1;
+          const float4* pp4 = reinterpret_cast<const float4*>(Pp_b + m * kBV + 20 * qq);
+          const float4* pm4 = reinterpret_cast<const float4*>(P_b + m * kBV + 20 * qq);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 kvc = kv[c4], kx = kh4[c4], qx = qx4[c4], pp = pp4[c4], pm = pm4[c4];
+            const float kvs[4] = {kvc.x, kvc.y, kvc.z, kvc.w};
+            const float khs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            const float pps[4] = {pp.x, pp.y, pp.z, pp.w}, pms[4] = {pm.x, pm.y, pm.z, pm.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pa = __fmaf_rn(kvs[e], __fmul_rn(pps[e], khs[e]), pa);
+              pb = __fmaf_rn(kvs[e], __fmul_rn(pms[e], qxs[e]), pb);
+            }
+          }
+        } else if (job < nrec + p.C) {
+          const int c = job - nrec;
+          const int id = cid[c];
+          const float4* b4 = reinterpret_cast<const float4*>(cl + (FIT ? (2 * c + 1) * kD : c * kD) + 16 * qq);
+          const float4* p04 = reinterpret_cast<const float4*>(Pp_b + 20 * qq);
+          const float4* a04 = reinterpret_cast<const float4*>(P_b + 20 * qq);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 bb = b4[c4], kx = kh4[c4], qx = qx4[c4], p0 = p04[c4], a0 = a04[c4];
+            float bs[4] = {bb.x, bb.y, bb.z, bb.w};
+            const float khs[4] = {kx.x, kx.y, kx.z, kx.w}, qxs[4] = {qx.x, qx.y, qx.z, qx.w};
+            const float p0s[4] = {p0.x, p0.y, p0.z, p0.w}, a0s[4] = {a0.x, a0.y, a0.z, a0.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!FIT && id >= kD) bs[e] = (16 * qq + 4 * c4 + e == id - kD) ? 1.0f : 0.0f;
+              pa = __fmaf_rn(bs[e], __fmul_rn(p0s[e], khs[e]), pa);
+              pb = __fmaf_rn(bs[e], __fmul_rn(a0s[e], qxs[e]), pb);
+            }
+          }
+        } else {
+          // the erase key (record n, P_n = 1) or the write key (record n+1) against r
+          const float4* x4 = reinterpret_cast<const float4*>((job == nrec + p.C ? en_b : kn_b) + 20 * qq);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 x = x4[c4], qx = qx4[c4];
+            pb = __fmaf_rn(x.x, qx.x, pb);
+            pb = __fmaf_rn(x.y, qx.y, pb);
+            pb = __fmaf_rn(x.z, qx.z, pb);
+            pb = __fmaf_rn(x.w, qx.w, pb);
+          }
+        }
+      }
+      pa = tree8(pa);
+      pb = tree8(pb);
+      if (job < njobs && qq == 0) {
+        if (job < nrec) {
+          g[job] = pa;
+          h[job] = pb;
+        } else if (job < nrec + p.C) {
+          ec[job - nrec] = pa;
+          eq[job - nrec] = pb;
+        } else {
+          h[job - p.C] = pb;  // h[n-1]: the erase key, h[n]: the write key
+        }
+      }
+    }
+  }
+
+  // The read and the output: two chains per code.
+  {
+    const int8_t* cb = at<int8_t>(sm, L.codes);
+    const float4* zk4 = reinterpret_cast<const float4*>(zk_b + 20 * qq);
+    const float4* zq4 = reinterpret_cast<const float4*>(zq_b + 20 * qq);
+    float v[2 * RPT];
+#pragma unroll
+    for (int half = 0; half < RPT / 4; ++half) {
+      uint32_t cw[4][4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+        code_words<BITS>(cb + ((4 * half + pp) * 4 * NW + 4 * w + r) * row_bytes<BITS>(), qq, cw[pp]);
+      float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aqq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 a = zk4[c4], b = zq4[c4];
+        const float za[4] = {a.x, a.y, a.z, a.w}, zb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f = code_at<BITS>(cw[pp], 4 * c4 + e);
+            ak[pp] = __fmaf_rn(f, za[e], ak[pp]);
+            aqq[pp] = __fmaf_rn(f, zb[e], aqq[pp]);
+          }
+        }
+      }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        v[4 * half + pp] = ak[pp];
+        v[RPT + 4 * half + pp] = aqq[pp];
+      }
+    }
+    float tot[2 * RPT / 8];
+    tree_transpose<2 * RPT>(v, qq, tot);
+    const int b0 = qq & 1, b1 = (qq >> 1) & 1, b2 = (qq >> 2) & 1;
+    float* dst = b0 ? baseq : basek;
+#pragma unroll
+    for (int e = 0; e < 2 * RPT / 8; ++e) {
+      const int pp = (RPT / 2) * b1 + (RPT / 4) * b2 + e;
+      const int i = pp * 4 * NW + 4 * w + r;
+      dst[i] = __fmul_rn(sg[i], tot[e]);
+    }
+  }
+  __syncthreads();
+
+  // Rows: the read (base, compensators, records) gives u_e = -read; the output
+  // adds the erase record and then the pure write.
+  if (tid < kD) {
+    const int i = tid;
+    const float* ru = at<float>(sm, L.rec_u);
+    const int64_t rec_off = (s * p.W + (n - 1)) * kD;
+    float acc = basek[i], oo = baseq[i];
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      if (c < p.C) {
+        const int id = cid[c];
+        const float a = FIT ? cl[2 * c * kD + i] : (id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f));
+        acc = __fmaf_rn(a, ec[c], acc);
+        oo = __fmaf_rn(a, eq[c], oo);
+      }
+    }
+    const float* rui = ru + i;
+    for (int m0 = 0; m0 < n - 1; m0 += 4) {
+      const float4 g4 = *reinterpret_cast<const float4*>(g + m0);
+      const float4 h4 = *reinterpret_cast<const float4*>(h + m0);
+      const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, hs[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (m0 + e < n - 1) {
+          const float um = rui[(m0 + e) * kD];
+          acc = __fmaf_rn(um, gs[e], acc);
+          oo = __fmaf_rn(um, hs[e], oo);
+        }
+      }
+    }
+    const float ue = -acc;
+    oo = __fmaf_rn(ue, h[n - 1], oo);
+    oo = __fmaf_rn(tk.v, h[n], oo);
+    p.rec_u[rec_off + i] = ue;
+    p.rec_u[rec_off + kD + i] = tk.v;
+    p.rec_k[rec_off + i] = en_b[bv(i)];
+    p.rec_k[rec_off + kD + i] = tk.k;
+    p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + i] = tk.a;
+    p.rec_alpha[s * p.alpha_stride + n * kD + i] = 1.0f;
+    p.o[s * kD + i] = oo;
   }
 }
 
@@ -2084,6 +2328,40 @@ __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
   }
 }
 
+// RWKV7 tokens (lq_decode_step_rwkv7): erase and pure-write records in one pass.
+template <int BITS, bool FIT>
+__global__ void __launch_bounds__(128, 8) k_append_rwkv(Params p) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ StageInfo s_info;
+  const int64_t s = blockIdx.x;
+  const int slots = append2_slots(p.W, p.phase);
+  const Stage& L = p.st;
+  const int known = (p.phase >= 0 && p.phase <= p.W - 2) ? p.phase : -1;
+  const TokenRegs tk = load_token(p, s);
+  float khv = 0.0f, kav = 0.0f;
+  if (threadIdx.x < kD) {
+    khv = p.kh[s * kD + threadIdx.x];
+    kav = p.ka[s * kD + threadIdx.x];
+  }
+  float4 kpre[4];
+  if (known >= 0) prefetch_key(p, s, known, kpre);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
+  if (known < 0) prefetch_key(p, s, si.issued, kpre);
+  const int n0 = stage_finish(p, s, &bar, si, true, 0, 2);
+  if (n0 < 0) return;
+  append_rwkv_compute<BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, tk, khv, kav, kpre);
+  if (threadIdx.x == 0) {
+    p.counts[s] = n0 + 2;
+    if (p.push_full && n0 + 2 == p.W) {
+      const int slot = atomicAdd(&p.hdr->full_n, 1);
+      if (slot >= 0 && slot < p.n_states)
+        p.full_list[slot] = (int32_t)s;
+      else
+        set_error(p, LQ_ERR_STATE, s);
+    }
+  }
+}
+
 // Append, then -- when that fills the window -- fold while the state is on chip.
 template <bool KDA, int BITS, bool FIT>
 __global__ void __launch_bounds__(256, 3) k_step(Params p) {
@@ -2276,10 +2554,10 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
 // launchers
 
 static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile,
-                          bool two = false) {
+                          bool two = false, bool rwkv = false) {
   Params q = p;
   q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits, p.comp_fit,
-                      two);
+                      two, rwkv);
   q.r1 = tile ? region1_bytes(q.st) : q.st.end;
   return q;
 }
@@ -2338,6 +2616,18 @@ cudaError_t launch_append2(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true);
   return launch(LQ_PICK2(k_append2, q), q, smem_of(q, false), st, 128);
 }
+
+// Kernel K<BITS, FIT> (per-key decay only) for this configuration.
+#define LQ_PICK_R(K, q) \
+  ((q).bits == 4 ? ((q).comp_fit > 0 ? K<4, true> : K<4, false>) \
+                 : ((q).bits == 6 ? ((q).comp_fit > 0 ? K<6, true> : K<6, false>) \
+                                  : ((q).comp_fit > 0 ? K<8, true> : K<8, false>)))
+
+cudaError_t launch_append_rwkv(const Params& p, cudaStream_t st) {
+  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true, true);
+  return launch(LQ_PICK_R(k_append_rwkv, q), q, smem_of(q, false), st, 128);
+}
+#undef LQ_PICK_R
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
   const Params q = with_layout(p, p.W, p.W, true, true, true);

@@ -29,8 +29,8 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
 
 # Every symbol include/lq.h declares.
 EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_state_init_range", "lq_append",
-           "lq_fold", "lq_decode_step", "lq_decode_step2", "lq_export_state", "lq_fp32_decode_step",
-           "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
+           "lq_fold", "lq_decode_step", "lq_decode_step2", "lq_decode_step_rwkv7", "lq_export_state",
+           "lq_fp32_decode_step", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
 
 
 class Config(ctypes.Structure):
@@ -83,6 +83,7 @@ def load():
         "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
         "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
         "lq_decode_step2": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P, P, P, P]),
+        "lq_decode_step_rwkv7": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P, P]),
         "lq_export_state": (ctypes.c_int, [cfgp, P, i64, P, P]),
         "lq_fp32_decode_step": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_get_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), P]),
@@ -205,6 +206,14 @@ def decode_step2(cfg, state, n_states, q, k1, v1, beta1, k2, v2, beta2, alpha, o
                                   _ptr(k1, "k1", f), _ptr(v1, "v1", f), _ptr(beta1, "beta1", f), _ptr(k2, "k2", f),
                                   _ptr(v2, "v2", f), _ptr(beta2, "beta2", f), _ptr(alpha, "alpha", f),
                                   _ptr(o, "o", f), _stream(stream)))
+
+
+def decode_step_rwkv7(cfg, state, n_states, r, w, kh, a, k, v, o, phase=PHASE_ANY, stream=None):
+    """One RWKV7 token: the erase record (a . kh, -(S kh), w), then the pure write (k, v, 1); o = S r."""
+    f = _f32()
+    _check(load().lq_decode_step_rwkv7(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(phase),
+                                       _ptr(r, "r", f), _ptr(w, "w", f), _ptr(kh, "kh", f), _ptr(a, "a", f),
+                                       _ptr(k, "k", f), _ptr(v, "v", f), _ptr(o, "o", f), _stream(stream)))
 
 
 def export_state(cfg, state, n_states, S_out, stream=None):

@@ -157,6 +157,10 @@ def test_invalid_sizes_and_nulls_rejected_on_host(L):
     one = lq.default_config()
     one.window = 1
     assert step2(one, -1) == lq.ERR_UNSUPPORTED
+    rwkv = lambda c, ph: L.lq_decode_step_rwkv7(ctypes.byref(c), None, 0, ph, *([None] * 8))
+    kda = lq.config(kda=True)
+    assert rwkv(kda, -1) == lq.OK and rwkv(kda, 14) == lq.OK and rwkv(kda, 15) == lq.ERR_INVALID_ARG
+    assert rwkv(cfg, -1) == lq.ERR_UNSUPPORTED  # scalar decay
 
 
 def test_error_message_is_thread_local(L):
