@@ -5,19 +5,22 @@
  * The method: LeapQuant (paperlayer.ai summary of arXiv 2609.38166v1). Each
  * head-state S (d_v x d_k = 128 x 128; row i = value channel, column j = key
  * channel) is held as
- *   - int8 codes with one fp32 step per value row (sigma),
+ *   - 8-bit codes (or 6- or 4-bit, lq_config.code_bits) with one fp32 step per
+ *     value row (sigma),
  *   - one fp32 smoothing scale per key channel (lambda; §3.4 Residual smoothing),
- *   - C fp32 Compensator Tokens, each one whole row or column of the state
- *     (§3.3 Compensator Tokens),
+ *   - C fp32 Compensator Tokens, each one whole row or column of the state, or
+ *     with lq_config.comp_fit a fitted rank-one factor pair (§3.3 Compensator
+ *     Tokens),
  * fixed for a window of W tokens (§3.2 Per-window quantization), plus a buffer
  * of up to W fp32 records (k_m, u_m, alpha_m), one per token of the open window.
  * Per token, the append step reads the state from the fixed boundary plus the
  * records (App. B.2 window unrolling, App. B.3 readout with a smoothed
  * quantized residual), forms the delta-rule correction u, stores the record and
  * writes the output. When the window is full, the fold rebuilds the state in
- * original coordinates, selects compensators, smooths, rounds once to int8 and
- * empties the buffer (fastpathlabs.ai research note 4, "What we built": an
- * append step and a fold).
+ * original coordinates, selects (or fits) compensators, smooths, rounds once
+ * and empties the buffer (fastpathlabs.ai research note 4, "What we built": an
+ * append step and a fold). Tokens whose update takes two rank-one sub-steps
+ * (DeltaProduct with two steps, RWKV7) leave two records (App. A).
  *
  * Conventions for every call below:
  *   - Ownership: the caller owns every buffer. The library allocates no memory

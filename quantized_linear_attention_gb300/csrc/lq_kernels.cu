@@ -5,17 +5,24 @@
 // unrolling and App. B.3 readout with a smoothed quantized residual. The append /
 // fold split follows fastpathlabs.ai research note 4, "What we built".
 //
-// One CTA owns one head-state. Work is bandwidth-bound matvec plus rank-one
-// terms, so it runs on the CUDA cores; no tensor cores.
+// Kernels: k_append (one record per token), k_append2 (two records: a
+// DeltaProduct token with two steps), k_append_rwkv (an RWKV7 token: erase and
+// pure-write records), k_step (one record, then the fold in the same CTA when
+// the window fills), k_fold_listed (persistent: folds the windows a mixed-phase
+// step filled), k_fold, k_export, k_init. One CTA owns one head-state (the
+// list fold walks a list of them). Work is matvec plus rank-one terms in a
+// pinned fp32 order, so it runs on the CUDA cores; no tensor cores. Codes are
+// 8, 6 or 4 bits (template parameter BITS).
 //
-// Data movement: right after reading the record count (or at once, when the
-// caller states the window phase), one thread issues bulk asynchronous copies
-// (cp.async.bulk, the TMA engine's 1-D form) of every byte the head-state needs
-// -- int8 codes, scales, compensators, buffered records, the token's q/k/v --
-// into shared memory on one mbarrier. All other arithmetic then reads shared
-// memory; global memory sees one burst of reads and the final writes. Waits on
-// the mbarrier are bounded (kWaitNs); on timeout the kernel records
-// LQ_ERR_TIMEOUT in the state's status word and leaves the head-state unchanged.
+// Data movement: at once when the caller states the window phase, else right
+// after reading the record count, one thread issues bulk asynchronous copies
+// (cp.async.bulk, the TMA engine's 1-D form) of the head-state's boundary
+// (codes, scales, compensators) and buffered records into shared memory on one
+// mbarrier; the token's inputs and (in the append kernels) the record keys are
+// read straight into registers meanwhile. Global memory sees one burst of
+// reads and the final writes. Waits on the mbarrier are bounded (kWaitNs); on
+// timeout the kernel records LQ_ERR_TIMEOUT in the state's status word and
+// leaves the head-state unchanged.
 //
 // Fixed evaluation order. Every value that feeds the stored state (u, decay
 // products, the per-entry fold chain, line scores, lambda, sigma, codes) is
