@@ -1787,21 +1787,62 @@ __device__ __forceinline__ float fit_dot(const float* a, const float* b) {
 
 // Modified Gram-Schmidt over V [C][128] in order: each vector loses its
 // components along the earlier ones (fma per entry), then is normalized
-// through one reciprocal of its length; a zero vector stays zero.
+// through one reciprocal of its length; a zero vector stays zero. Warp 0 does
+// it alone (its four lane groups form each dot product), then one barrier.
 __device__ __forceinline__ void fit_orthonormalize(float* V, int C) {
-  const int tid = threadIdx.x;
-  for (int c = 0; c < C; ++c) {
-    float* v = V + c * kD;
-    for (int e = 0; e < c; ++e) {
-      const float d = fit_dot(v, V + e * kD);
-      __syncthreads();
-      if (tid < kD) v[tid] = __fmaf_rn(-d, V[e * kD + tid], v[tid]);
-      __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    for (int c = 0; c < C; ++c) {
+      float* v = V + c * kD;
+      for (int e = 0; e < c; ++e) {
+        const float d = fit_dot(v, V + e * kD);
+        __syncwarp();
+#pragma unroll
+        for (int j = lane; j < kD; j += 32) v[j] = __fmaf_rn(-d, V[e * kD + j], v[j]);
+        __syncwarp();
+      }
+      const float inv = fit_inv_norm(v);
+      __syncwarp();
+#pragma unroll
+      for (int j = lane; j < kD; j += 32) v[j] = __fmul_rn(v[j], inv);
+      __syncwarp();
     }
-    const float inv = fit_inv_norm(v);
-    __syncthreads();
-    if (tid < kD) v[tid] = __fmul_rn(v[tid], inv);
-    __syncthreads();
+  }
+  __syncthreads();
+}
+
+// Y[c] = R v_c for every factor c < C in one walk over the tile (the row walk's
+// order per factor); thread (w, r, qq) as in fit_row_walk.
+__device__ __forceinline__ void fit_row_walk_all(const float* S, const float* V, int C, float* Y,
+                                                 const int roff[4]) {
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {
+    const int i = 32 * pp + 4 * w + r;
+    float x[16];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 t = *reinterpret_cast<const float4*>(&S[i * kD + roff[c4]]);
+      x[4 * c4] = t.x;
+      x[4 * c4 + 1] = t.y;
+      x[4 * c4 + 2] = t.z;
+      x[4 * c4 + 3] = t.w;
+    }
+    for (int c = 0; c < C; ++c) {
+      const float4* v4 = reinterpret_cast<const float4*>(V + c * kD + 16 * qq);
+      float acc = 0.0f;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 b = v4[c4];
+        acc = __fmaf_rn(x[4 * c4 + 0], b.x, acc);
+        acc = __fmaf_rn(x[4 * c4 + 1], b.y, acc);
+        acc = __fmaf_rn(x[4 * c4 + 2], b.z, acc);
+        acc = __fmaf_rn(x[4 * c4 + 3], b.w, acc);
+      }
+      acc = tree8(acc);
+      if (qq == 0) Y[c * kD + i] = acc;
+    }
   }
 }
 
@@ -1874,16 +1915,26 @@ __device__ __forceinline__ void fit_block_tile(const Params& p, int64_t s, float
     if (!keep && tid < kD) V[c * kD + tid] = S[sidx(s_rows[c], tid)];
   }
   __syncthreads();
+  // With C <= 4 the reads R v_c of a sweep share one walk (Y in the score arrays).
+  const bool fused = C <= 4;
+  float* Y = tl.score;
   for (int sw = 0; sw < p.comp_fit; ++sw) {
     fit_orthonormalize(V, C);
-    for (int c = 0; c < C; ++c) {
-      fit_row_walk(S, V + c * kD, 1.0f, y, roff);
+    if (fused) {
+      fit_row_walk_all(S, V, C, Y, roff);
       __syncthreads();
+    }
+    for (int c = 0; c < C; ++c) {
+      const float* yc = fused ? Y + c * kD : y;
+      if (!fused) {
+        fit_row_walk(S, V + c * kD, 1.0f, y, roff);
+        __syncthreads();
+      }
       float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
       const float* base = S + 16 * cb * kD;
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        const float ai = y[16 * cb + t];
+        const float ai = yc[16 * cb + t];
         const float4 x = *reinterpret_cast<const float4*>(base + t * kD + coff[t & 7]);
         c0 = __fmaf_rn(x.x, ai, c0);
         c1 = __fmaf_rn(x.y, ai, c1);
