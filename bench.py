@@ -731,6 +731,22 @@ def run_ours(args):
             "token_us_mean": round(1e3 * r_total / n_tok, 2),
             "append_us": round(1e3 * statistics.mean(r_app), 2),
             "fold_token_us": round(1e3 * statistics.mean(r_fold), 2)}
+    if rank == 0 and not args.no_kda:
+        kwl = wlm.WORKLOADS[5]
+        k_total, k_app, k_fold, _ = time_main(kwl, args, device, 1, 0, steps=20)
+        kN, kW = kwl.n_states, kwl.W
+        kb = kN * alg_bytes_window(kW, kwl.C, True)
+        k_app_bytes = kN * statistics.mean(alg_bytes_append(p, kwl.C, True) for p in range(kW - 1))
+        k_app_ms = statistics.mean(k_app)
+        result["kda_config5"] = {
+            "note": f"{kwl.name}: {kN} head-states with per-key decay, Student-t(3) values; 20 timed windows",
+            "head_tokens_per_s": round(kN * kW * 20 / (k_total / 1e3), 1),
+            "append_step_us": round(k_app_ms * 1e3, 2), "fold_step_us": round(statistics.mean(k_fold) * 1e3, 2),
+            "alg_bytes_per_head_token": round(kb / kN / kW, 1),
+            "window_gbs": round(kb / (k_total / 20 / 1e3) / 1e9, 1),
+            "window_frac": round(kb / (k_total / 20 / 1e3) / 1e9 / hbm, 4),
+            "append_gbs": round(k_app_bytes / (k_app_ms / 1e3) / 1e9, 1),
+            "append_frac": round(k_app_bytes / (k_app_ms / 1e3) / 1e9 / hbm, 4)}
     for bits in (6, 4):
         if rank != 0 or args.no_bits4:
             break
@@ -853,6 +869,7 @@ def main(argv=None):
     ap.add_argument("--no-fit", action="store_true", help="skip the fitted-factor compensator run")
     ap.add_argument("--no-stagger", action="store_true", help="skip the mixed-window-phase run")
     ap.add_argument("--no-two", action="store_true", help="skip the two-record-token and RWKV7 runs")
+    ap.add_argument("--no-kda", action="store_true", help="skip the per-key-decay (KDA) workload run")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
