@@ -44,6 +44,7 @@ METRIC = "head-tokens/s and achieved HBM GB/s (% of GB300 peak) at batch 32/128/
 UNIT = "head-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_append_gdn_batch128.md")
+PROFILE_STEP = os.path.join(ROOT, "profiles", "k_step_gdn_batch128.md")
 KERNEL_SOURCE = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc", "lq_kernels.cu")
 
 
@@ -122,13 +123,13 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def profile_traffic(n_states):
-    """(DRAM bytes per launch at n_states, note) from the committed ncu summary of the
-    dominant kernel, scaled from the captured head-states (traffic grows in
-    proportion to them), or (None, why) when there is none or the kernel source
-    changed since it was taken."""
+def profile_traffic(n_states, summary=PROFILE_SUMMARY):
+    """(DRAM bytes per launch at n_states, note) from a committed ncu summary (the
+    dominant kernel's by default), scaled from the captured head-states (traffic
+    grows in proportion to them), or (None, why) when there is none or the kernel
+    source changed since it was taken."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(summary).read()
     except OSError:
         return None, "no ncu summary committed"
     fields = {}
@@ -656,6 +657,10 @@ def run_ours(args):
     traffic, traffic_note = profile_traffic(N)
     fold_bytes = N * (alg_bytes_append(W - 1, wl.C, wl.kda) + alg_bytes_fold_extra(wl.C))
     win_bytes = N * alg_bytes_window(W, wl.C, wl.kda)
+    step_traffic, _ = profile_traffic(N, PROFILE_STEP)
+    win_dram = None
+    if traffic is not None and step_traffic is not None:  # 15 appends (phase-averaged) and the fold step
+        win_dram = round(((W - 1) * traffic + step_traffic) / N / W, 1)
     win_gbs = win_bytes / (t_ms / K / 1e3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -673,7 +678,10 @@ def run_ours(args):
                       "fold_cost_per_token_ms": round((fold_ms - app_ms) / W, 5),
                       "amortized_below_one_append": (fold_ms - app_ms) / W < app_ms},
         "window": {"alg_bytes": win_bytes, "achieved_gbs": round(win_gbs, 1), "frac": round(win_gbs / hbm, 4),
-                   "alg_bytes_per_head_token": round(win_bytes / N / W, 1)},
+                   "alg_bytes_per_head_token": round(win_bytes / N / W, 1),
+                   "ncu_dram_bytes_per_head_token": win_dram,
+                   "int8_state_minimum_per_head_token": 128 * 128 + 128 * 128 // W,
+                   "fp32_state_per_head_token": alg_bytes_fp32(wl.kda)},
         "gpu_launches": K * W,
         "clocks": clocks,
     }
