@@ -299,6 +299,7 @@ __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
 // at float 20b, so the eight lanes of a lane group, each reading its own block
 // with 16-byte loads, touch 32 distinct banks.
 constexpr int kBV = 160;
+constexpr int kAPre = 16;  // records whose per-key decays the append keeps in registers
 __host__ __device__ __forceinline__ int bv(int j) { return j + ((j >> 4) << 2); }
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
@@ -308,7 +309,7 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 // into registers, not staged.
 __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id_stride, int slots_u, int slots_k,
                                               bool append, bool fold, int bits, int comp_fit, bool two = false,
-                                              bool rwkv = false) {
+                                              bool rwkv = false, bool stage_alpha = true) {
   Stage L;
   int o = 0;
   auto take = [&](int bytes) {
@@ -324,7 +325,7 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.comp_line = take(4 * kD * C * (comp_fit > 0 ? 2 : 1));
   L.rec_k = take(4 * kD * slots_k);
   L.rec_u = take(4 * kD * slots_u);
-  L.rec_alpha = take(kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
+  L.rec_alpha = take(!stage_alpha ? 0 : kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
   L.kn_b = take(va * 4 * kBV);
   L.qn_b = take(va * 4 * kBV);
   L.zk_b = take(va * 4 * kBV);
@@ -397,13 +398,13 @@ namespace lqi {
 // Staging: one thread issues every copy of head-state s (n0 records held) on
 // `bar`, with the exact byte count announced first.
 __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, const Stage& L, char* sm,
-                                            uint64_t* bar, bool stage_k) {
+                                            uint64_t* bar, bool stage_k, bool stage_a = true) {
   const uint32_t rec = 4u * kD * (uint32_t)n0;
   const uint32_t alpha_bytes = p.kda ? rec : 4u * (uint32_t)p.alpha_stride;
   const uint32_t code_bytes = (uint32_t)(kD * kD * p.bits / 8);
   const uint32_t comp_floats = (uint32_t)(kD * p.C * (p.comp_fit > 0 ? 2 : 1));
   uint32_t bytes = code_bytes + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * comp_floats + rec;
-  if (!p.kda || n0 > 0) bytes += alpha_bytes;
+  if (stage_a && (!p.kda || n0 > 0)) bytes += alpha_bytes;
   if (stage_k) bytes += rec;
   mbar_expect_tx(bar, bytes);
   bulk_g2s(sm + L.codes, p.codes + s * code_bytes, code_bytes, bar);
@@ -415,7 +416,7 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
     if (stage_k) bulk_g2s(sm + L.rec_k, p.rec_k + s * p.W * kD, rec, bar);
     bulk_g2s(sm + L.rec_u, p.rec_u + s * p.W * kD, rec, bar);
   }
-  if (!p.kda || n0 > 0) bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
+  if (stage_a && (!p.kda || n0 > 0)) bulk_g2s(sm + L.rec_alpha, p.rec_alpha + s * p.alpha_stride, alpha_bytes, bar);
 }
 
 // Decay products from staged alphas (records 1..n-1, then alpha_n = the current
@@ -496,11 +497,13 @@ __device__ __forceinline__ TokenRegs load_token(const Params& p, int64_t s) {
 
 // KPRE: record keys are not staged; lane group g arrives with block qq of
 // record slot g in `kpre` (read before the staging wait), and slots beyond the
-// first round of lane groups are read from global memory.
+// first round of lane groups are read from global memory. With KDA the
+// records' decays are not staged either: thread j arrives with column j of the
+// first kAPre records in `apre` and reads the rest from global memory.
 template <bool KDA, int NT, bool FOLD, bool KPRE, int BITS, bool FIT>
 __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                float alpha_scalar, float beta, const TokenRegs& tk,
-                                               const float4 (&kpre)[4]) {
+                                               const float4 (&kpre)[4], const float (&apre)[kAPre]) {
   constexpr int NW = NT / 32;
   constexpr int RPT = 128 / (4 * NW);  // rows per thread: 8 or 4
   constexpr int NG = NT / 8;           // lane groups
@@ -533,9 +536,25 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       const int jb = bv(tid);
       float pr = 1.0f;
       P_b[n * kBV + jb] = pr;
-      for (int m = n; m >= 1; --m) {
-        pr = __fmul_rn(pr, m == n ? tk.a : ra[(m - 1) * kD + tid]);
-        P_b[(m - 1) * kBV + jb] = pr;
+      if (KPRE) {
+        pr = __fmul_rn(pr, tk.a);
+        P_b[(n - 1) * kBV + jb] = pr;
+        for (int m = n - 1; m > kAPre; --m) {
+          pr = __fmul_rn(pr, p.rec_alpha[s * p.alpha_stride + (m - 1) * kD + tid]);
+          P_b[(m - 1) * kBV + jb] = pr;
+        }
+#pragma unroll
+        for (int m = kAPre; m >= 1; --m) {
+          if (m <= n - 1) {
+            pr = __fmul_rn(pr, apre[m - 1]);
+            P_b[(m - 1) * kBV + jb] = pr;
+          }
+        }
+      } else {
+        for (int m = n; m >= 1; --m) {
+          pr = __fmul_rn(pr, m == n ? tk.a : ra[(m - 1) * kD + tid]);
+          P_b[(m - 1) * kBV + jb] = pr;
+        }
       }
     }
   } else {
@@ -2246,16 +2265,16 @@ struct StageInfo {
 
 __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int known_n0, const Stage& L,
                                                  uint64_t* bar, StageInfo* sh, bool stage_k, int max_n0,
-                                                 bool init_bar = true) {
+                                                 bool init_bar = true, bool stage_a = true) {
   if (threadIdx.x == 0) {
     if (init_bar) mbar_init(bar, 1);
     int n0 = known_n0;
-    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k);
+    if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k, stage_a);
     const int c = p.counts[s];
     const int h = header_ok(p) ? 1 : 0;
     if (n0 < 0) {
       n0 = (h && c >= 0 && c <= max_n0) ? c : -1;
-      if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k);
+      if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k, stage_a);
     }
     sh->issued = n0;
     sh->cnt = c;
@@ -2300,6 +2319,14 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
 // lq_append. With a stated phase the staging area holds exactly `phase` records.
 __host__ __device__ inline int append_slots(int W, int phase) { return (phase >= 0 && phase < W) ? phase : W - 1; }
 
+// Thread j's column of the first kAPre records' decays (KDA), of the n0 held.
+__device__ __forceinline__ void prefetch_alpha(const Params& p, int64_t s, int n0, float (&apre)[kAPre]) {
+  const int j = threadIdx.x;
+#pragma unroll
+  for (int m = 0; m < kAPre; ++m)
+    if (m < n0 && j < kD) apre[m] = p.rec_alpha[s * p.alpha_stride + m * kD + j];
+}
+
 // Lane group grp's block of record slot grp's key, when that slot is one of
 // the n0 records held.
 __device__ __forceinline__ void prefetch_key(const Params& p, int64_t s, int n0, float4 (&kpre)[4]) {
@@ -2316,7 +2343,7 @@ __device__ __forceinline__ void prefetch_key(const Params& p, int64_t s, int n0,
 // else once thread 0 has read the record count. With p.push_full the
 // head-states whose window this token fills are put on the full-window list.
 template <bool KDA, int BITS, bool FIT>
-__global__ void __launch_bounds__(128, 8) k_append(Params p) {
+__global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -2327,12 +2354,19 @@ __global__ void __launch_bounds__(128, 8) k_append(Params p) {
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
   const TokenRegs tk = load_token(p, s);
   float4 kpre[4];
-  if (known >= 0) prefetch_key(p, s, known, kpre);
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
-  if (known < 0) prefetch_key(p, s, si.issued, kpre);
+  float apre[kAPre];
+  if (known >= 0) {
+    prefetch_key(p, s, known, kpre);
+    if (KDA) prefetch_alpha(p, s, known, apre);
+  }
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots, true, !KDA);
+  if (known < 0) {
+    prefetch_key(p, s, si.issued, kpre);
+    if (KDA) prefetch_alpha(p, s, si.issued, apre);
+  }
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
-  append_compute<KDA, 128, false, true, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 128, false, true, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta, tk, kpre, apre);
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 1;
     if (p.push_full && n0 + 1 == p.W) {
@@ -2432,16 +2466,17 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   const int known = (p.phase >= 0 && p.phase < p.W) ? p.phase : -1;
   const TokenRegs tk = load_token(p, s);
   float4 kpre[4];
+  float apre[kAPre];
   const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, p.W - 1);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;
   if (n < p.W) {
-    append_compute<KDA, 256, false, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+    append_compute<KDA, 256, false, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre, apre);
     if (threadIdx.x == 0) p.counts[s] = n;
     return;
   }
-  append_compute<KDA, 256, true, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre);
+  append_compute<KDA, 256, true, false, BITS, FIT>(p, s, n, L, lq_dyn_smem, alpha_s, beta, tk, kpre, apre);
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
@@ -2612,10 +2647,10 @@ __global__ void __launch_bounds__(256, 3) k_init(Params p) {
 // launchers
 
 static Params with_layout(const Params& p, int slots_u, int slots_k, bool append, bool fold, bool tile,
-                          bool two = false, bool rwkv = false) {
+                          bool two = false, bool rwkv = false, bool stage_alpha = true) {
   Params q = p;
   q.st = stage_layout(p.W, p.C, p.kda, (int)p.comp_id_stride, slots_u, slots_k, append, fold, p.bits, p.comp_fit,
-                      two, rwkv);
+                      two, rwkv, stage_alpha);
   q.r1 = tile ? region1_bytes(q.st) : q.st.end;
   return q;
 }
@@ -2666,7 +2701,7 @@ cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st) {
 // Staging holds `phase` records (W-1 when the phase is not stated); the keys
 // travel in registers.
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, append_slots(p.W, p.phase), 0, true, false, false);
+  const Params q = with_layout(p, append_slots(p.W, p.phase), 0, true, false, false, false, false, !p.kda);
   return launch(LQ_PICK2(k_append, q), q, smem_of(q, false), st, 128);
 }
 
