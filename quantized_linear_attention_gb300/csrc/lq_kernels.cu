@@ -818,7 +818,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
 template <int BITS, bool FIT>
 __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                     const TokenRegs& tk, float khv, float kav,
-                                                    const float4 (&kpre)[4]) {
+                                                    const float4 (&kpre)[4], const float (&apre)[kAPre]) {
   constexpr int NW = 4, RPT = 8, NG = 16;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -851,12 +851,22 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
     P_b[(n - 1) * kBV + jb] = pr;
     float pp = 1.0f;
     Pp_b[(n - 1) * kBV + jb] = pp;
-    for (int m = n - 1; m >= 1; --m) {
-      const float am = ra[(m - 1) * kD + tid];
+    for (int m = n - 1; m > kAPre; --m) {
+      const float am = p.rec_alpha[s * p.alpha_stride + (m - 1) * kD + tid];
       pr = __fmul_rn(pr, am);
       P_b[(m - 1) * kBV + jb] = pr;
       pp = __fmul_rn(pp, am);
       Pp_b[(m - 1) * kBV + jb] = pp;
+    }
+#pragma unroll
+    for (int m = kAPre; m >= 1; --m) {
+      if (m <= n - 1) {
+        const float am = apre[m - 1];
+        pr = __fmul_rn(pr, am);
+        P_b[(m - 1) * kBV + jb] = pr;
+        pp = __fmul_rn(pp, am);
+        Pp_b[(m - 1) * kBV + jb] = pp;
+      }
     }
   }
   __syncthreads();
@@ -1059,7 +1069,8 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
 template <bool KDA, int BITS, bool FIT>
 __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int n, const Stage& L, char* sm,
                                                 float alpha_scalar, float beta1, float beta2, const TokenRegs& tk,
-                                                float k2v, float v2v, const float4 (&kpre)[4]) {
+                                                float k2v, float v2v, const float4 (&kpre)[4],
+                                                const float (&apre)[kAPre]) {
   constexpr int NW = 4, RPT = 8, NG = 16;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -1093,9 +1104,18 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
       const int jb = bv(tid);
       float pr = 1.0f;
       P_b[n * kBV + jb] = pr;
-      for (int m = n; m >= 1; --m) {
-        pr = __fmul_rn(pr, m == n ? tk.a : ra[(m - 1) * kD + tid]);
+      pr = __fmul_rn(pr, tk.a);
+      P_b[(n - 1) * kBV + jb] = pr;
+      for (int m = n - 1; m > kAPre; --m) {
+        pr = __fmul_rn(pr, p.rec_alpha[s * p.alpha_stride + (m - 1) * kD + tid]);
         P_b[(m - 1) * kBV + jb] = pr;
+      }
+#pragma unroll
+      for (int m = kAPre; m >= 1; --m) {
+        if (m <= n - 1) {
+          pr = __fmul_rn(pr, apre[m - 1]);
+          P_b[(m - 1) * kBV + jb] = pr;
+        }
       }
     }
   } else if (tid == 0) {
@@ -2386,7 +2406,7 @@ __host__ __device__ inline int append2_slots(int W, int phase) {
 }
 
 template <bool KDA, int BITS, bool FIT>
-__global__ void __launch_bounds__(128, 6) k_append2(Params p) {
+__global__ void __launch_bounds__(128, KDA ? 4 : 6) k_append2(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -2402,12 +2422,19 @@ __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
     v2v = p.v2[s * kD + threadIdx.x];
   }
   float4 kpre[4];
-  if (known >= 0) prefetch_key(p, s, known, kpre);
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
-  if (known < 0) prefetch_key(p, s, si.issued, kpre);
+  float apre[kAPre];
+  if (known >= 0) {
+    prefetch_key(p, s, known, kpre);
+    if (KDA) prefetch_alpha(p, s, known, apre);
+  }
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots, true, !KDA);
+  if (known < 0) {
+    prefetch_key(p, s, si.issued, kpre);
+    if (KDA) prefetch_alpha(p, s, si.issued, apre);
+  }
   const int n0 = stage_finish(p, s, &bar, si, true, 0, 2);
   if (n0 < 0) return;
-  append2_compute<KDA, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta1, beta2, tk, k2v, v2v, kpre);
+  append2_compute<KDA, BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, alpha_s, beta1, beta2, tk, k2v, v2v, kpre, apre);
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 2;
     if (p.push_full && n0 + 2 == p.W) {
@@ -2422,7 +2449,7 @@ __global__ void __launch_bounds__(128, 6) k_append2(Params p) {
 
 // RWKV7 tokens (lq_decode_step_rwkv7): erase and pure-write records in one pass.
 template <int BITS, bool FIT>
-__global__ void __launch_bounds__(128, 8) k_append_rwkv(Params p) {
+__global__ void __launch_bounds__(128, 4) k_append_rwkv(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -2436,12 +2463,19 @@ __global__ void __launch_bounds__(128, 8) k_append_rwkv(Params p) {
     kav = p.ka[s * kD + threadIdx.x];
   }
   float4 kpre[4];
-  if (known >= 0) prefetch_key(p, s, known, kpre);
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots);
-  if (known < 0) prefetch_key(p, s, si.issued, kpre);
+  float apre[kAPre];
+  if (known >= 0) {
+    prefetch_key(p, s, known, kpre);
+    prefetch_alpha(p, s, known, apre);
+  }
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, false, slots, true, false);
+  if (known < 0) {
+    prefetch_key(p, s, si.issued, kpre);
+    prefetch_alpha(p, s, si.issued, apre);
+  }
   const int n0 = stage_finish(p, s, &bar, si, true, 0, 2);
   if (n0 < 0) return;
-  append_rwkv_compute<BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, tk, khv, kav, kpre);
+  append_rwkv_compute<BITS, FIT>(p, s, n0 + 1, L, lq_dyn_smem, tk, khv, kav, kpre, apre);
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 2;
     if (p.push_full && n0 + 2 == p.W) {
@@ -2706,7 +2740,7 @@ cudaError_t launch_append(const Params& p, cudaStream_t st) {
 }
 
 cudaError_t launch_append2(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true);
+  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true, false, !p.kda);
   return launch(LQ_PICK2(k_append2, q), q, smem_of(q, false), st, 128);
 }
 
@@ -2717,7 +2751,7 @@ cudaError_t launch_append2(const Params& p, cudaStream_t st) {
                                   : ((q).comp_fit > 0 ? K<8, true> : K<8, false>)))
 
 cudaError_t launch_append_rwkv(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true, true);
+  const Params q = with_layout(p, append2_slots(p.W, p.phase), 0, true, false, false, true, true, false);
   return launch(LQ_PICK_R(k_append_rwkv, q), q, smem_of(q, false), st, 128);
 }
 #undef LQ_PICK_R
