@@ -253,7 +253,10 @@ def setup_state(wl, device, state0=0, bits=8, comp_fit=0, comp_block=0):
 
 
 def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0, comp_block=0):
-    """The timed region: K windows, a CUDA event between every two launches."""
+    """Two timed passes over whole windows. The headline pass records one CUDA event
+    before and one after its K windows (an event between launches costs about 2 us
+    a launch on the stream). The breakdown pass records an event between every two
+    launches, for the append and fold-step times."""
     import torch
 
     from quantized_linear_attention_gb300 import lq
@@ -275,30 +278,38 @@ def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0, c
             tok += 1
     torch.cuda.synchronize()
     K = args.steps if steps is None else steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K * W + 1)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device.index or 0)
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
     sampler.mark_start()
-    ev[0].record()
-    for i in range(K * W):
+    e0.record()
+    for _ in range(K * W):
         launch(tok)
         tok += 1
-        ev[i + 1].record()
+    e1.record()
     torch.cuda.synchronize()
     sampler.mark_end()
     barrier(world)
     clocks = sampler.stop()
+    total_ms = e0.elapsed_time(e1)
+    Kb = min(K, 100)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(Kb * W + 1)]
+    ev[0].record()
+    for i in range(Kb * W):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
     status, bad = lq.get_status(state)
     if status != lq.OK:
         raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
     if not torch.isfinite(o).all():
         raise RuntimeError("non-finite output")
-    total_ms = ev[0].elapsed_time(ev[-1])
-    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(K * W)]
-    app = [d[i] for i in range(K * W) if i % W != W - 1]
-    fold = [d[i] for i in range(K * W) if i % W == W - 1]
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(Kb * W)]
+    app = [d[i] for i in range(Kb * W) if i % W != W - 1]
+    fold = [d[i] for i in range(Kb * W) if i % W == W - 1]
     del state, pool
     torch.cuda.empty_cache()
     return total_ms, app, fold, clocks
