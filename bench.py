@@ -315,6 +315,29 @@ def time_main(wl, args, device, world, rank=0, bits=8, steps=None, comp_fit=0, c
     return total_ms, app, fold, clocks
 
 
+def two_passes(launch, tok, n_head, n_break):
+    """Run n_head launches between two CUDA events (the throughput), then n_break
+    launches with an event between every two (the per-launch times). Returns
+    (total ms of the first pass, per-launch ms of the second, next token)."""
+    import torch
+
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_head):
+        launch(tok)
+        tok += 1
+    e1.record()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_break + 1)]
+    ev[0].record()
+    for i in range(n_break):
+        launch(tok)
+        tok += 1
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), [ev[i].elapsed_time(ev[i + 1]) for i in range(n_break)], tok
+
+
 def time_staggered(wl, device, steps=50, warmup=3):
     """Head-states at W different window phases: group g (states g*N/W ..) is re-admitted
     by lq_state_init_range before token g, then every token is one lq_decode_step with
@@ -341,23 +364,15 @@ def time_staggered(wl, device, steps=50, warmup=3):
     for _ in range(warmup * W):
         launch(tok)
         tok += 1
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * W + 1)]
-    ev[0].record()
-    for i in range(steps * W):
-        launch(tok)
-        tok += 1
-        ev[i + 1].record()
-    torch.cuda.synchronize()
+    total, d, tok = two_passes(launch, tok, steps * W, min(steps, 20) * W)
     status, bad = lq.get_status(state)
     if status != lq.OK:
         raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
     counts = lq.state_views(cfg, state, N)["counts"]
     phases = torch.bincount(counts.long(), minlength=W).tolist()
-    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * W)]
     del state, pool
     torch.cuda.empty_cache()
-    return ev[0].elapsed_time(ev[-1]), d, phases
+    return total, d, phases
 
 
 def time_two_record(wl, device, steps=50, warmup=3):
@@ -383,23 +398,15 @@ def time_two_record(wl, device, steps=50, warmup=3):
     for _ in range(warmup * per_win):
         launch(tok)
         tok += 1
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * per_win + 1)]
-    ev[0].record()
-    for i in range(steps * per_win):
-        launch(tok)
-        tok += 1
-        ev[i + 1].record()
-    torch.cuda.synchronize()
+    total, d, tok = two_passes(launch, tok, steps * per_win, min(steps, 20) * per_win)
     status, bad = lq.get_status(state)
     if status != lq.OK:
         raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
-    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * per_win)]
     app = [d[i] for i in range(len(d)) if i % per_win != per_win - 1]
     fold = [d[i] for i in range(len(d)) if i % per_win == per_win - 1]
     del state, pool
     torch.cuda.empty_cache()
-    return ev[0].elapsed_time(ev[-1]), app, fold
+    return total, app, fold, steps * per_win
 
 
 def time_rwkv(device, steps=50, warmup=3):
@@ -429,23 +436,15 @@ def time_rwkv(device, steps=50, warmup=3):
     for _ in range(warmup * per_win):
         launch(tok)
         tok += 1
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps * per_win + 1)]
-    ev[0].record()
-    for i in range(steps * per_win):
-        launch(tok)
-        tok += 1
-        ev[i + 1].record()
-    torch.cuda.synchronize()
+    total, d, tok = two_passes(launch, tok, steps * per_win, min(steps, 20) * per_win)
     status, bad = lq.get_status(state)
     if status != lq.OK:
         raise RuntimeError(f"device status {lq.STATUS_NAMES.get(status)} at head-state {bad}")
-    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps * per_win)]
     app = [d[i] for i in range(len(d)) if i % per_win != per_win - 1]
     fold = [d[i] for i in range(len(d)) if i % per_win == per_win - 1]
     del state, pool
     torch.cuda.empty_cache()
-    return ev[0].elapsed_time(ev[-1]), app, fold
+    return total, app, fold, steps * per_win
 
 
 def time_graphed(wl, steps, device):
@@ -716,20 +715,21 @@ def run_ours(args):
     if rank == 0 and not args.no_stagger:
         s_total, s_d, phases = time_staggered(wl, device)
         s_sorted = sorted(s_d)
+        s_n = 50 * W
         result["staggered"] = {
             "note": f"{W} groups of {N // W} head-states, group g re-admitted from a zero state before token g "
                     "(lq_state_init_range), then "
                     "lq_decode_step with LQ_PHASE_ANY: each token appends every head-state, lists the windows it "
-                    f"fills and folds them (1/{W} of the head-states); 50 timed windows, 2 launches per token",
-            "head_tokens_per_s": round(N * len(s_d) / (s_total / 1e3), 1),
-            "step_us_mean": round(1e3 * s_total / len(s_d), 2), "step_us_max": round(1e3 * s_sorted[-1], 2),
+                    f"fills and folds them (1/{W} of the head-states); 50 timed windows, 2 launches per token; "
+                    "max and p50 from 20 more windows with an event between tokens",
+            "head_tokens_per_s": round(N * s_n / (s_total / 1e3), 1),
+            "step_us_mean": round(1e3 * s_total / s_n, 2), "step_us_max": round(1e3 * s_sorted[-1], 2),
             "step_us_p50": round(1e3 * s_sorted[len(s_d) // 2], 2),
             "in_phase_step_us_max": round(1e3 * max(fold), 2),
             "in_phase_step_us_mean": round(1e3 * t_ms / K / W, 2),
             "head_states_per_phase_after": phases}
     if rank == 0 and not args.no_two:
-        t_total, t_app, t_fold = time_two_record(wl, device)
-        n_tok = len(t_app) + len(t_fold)
+        t_total, t_app, t_fold, n_tok = time_two_record(wl, device)
         result["two_record"] = {
             "note": f"two-record tokens (DeltaProduct with two steps, lq_decode_step2): {W // 2} tokens per "
                     f"{W}-record window, one kernel per token reads the boundary once; the last token of a window "
@@ -740,8 +740,7 @@ def run_ours(args):
             "fold_token_us": round(1e3 * statistics.mean(t_fold), 2),
             "two_one_record_steps_us": round(2e3 * t_ms / K / W, 2)}
     if rank == 0 and not args.no_two:
-        r_total, r_app, r_fold = time_rwkv(device)
-        n_tok = len(r_app) + len(r_fold)
+        r_total, r_app, r_fold, n_tok = time_rwkv(device)
         result["rwkv7"] = {
             "note": "RWKV7 tokens (lq_decode_step_rwkv7: an erase record and a pure-write record, one kernel per "
                     f"token) on {N} head-states with per-key decay; {W // 2} tokens per {W}-record window, the "
