@@ -533,13 +533,16 @@ def time_fp32(wl, device, tokens=48, warmup=4):
     return ms
 
 
-def time_e2e(wl, steps, device, ring=4):
+def time_e2e(wl, steps, device, ring=8):
     """End to end through the C ABI with host buffers: every token's inputs are
     copied from pinned host memory and every token's output is copied back, all
     inside the timed region. The copies run on two side streams and overlap the
     decode calls, as a serving loop would: host-to-device for token t+1 while
     token t decodes, device-to-host of each output once its token is done
-    (a ring of `ring` token slots on the device, ordered by events)."""
+    (a ring of `ring` token slots on the device, ordered by events). A token's
+    inputs take longer to copy (about 120 us at 210 GB/s) than its append takes
+    to run (106 us), so the copies must run ahead through the window's fold
+    token: 8 slots let them, 4 did not (95 M against 108 M head-tokens/s)."""
     import torch
 
     from quantized_linear_attention_gb300 import lq
@@ -809,7 +812,7 @@ def run_ours(args):
         result["e2e"] = {"value": round(N * W * args.e2e_steps / (ms / 1e3), 1), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "note": "per token: pinned host inputs -> device and the output -> host on two side "
-                                 "streams, overlapping the lq_decode_step calls (a ring of 4 token slots)"}
+                                 "streams, overlapping the lq_decode_step calls (a ring of 8 token slots)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
