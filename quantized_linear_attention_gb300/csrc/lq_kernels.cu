@@ -213,6 +213,41 @@ __device__ __forceinline__ void tree_transpose(float v[Q], int qq, float out[Q /
   for (int e = 0; e < Q / 8; ++e) out[e] = v[e];
 }
 
+// x . y over the 128 key channels held one per thread (threads 0..127), as if
+// summed in twice the working precision and rounded once (the Dot2 scheme of
+// Ogita, Rump and Oishi, "Accurate sum and dot product", 2005): each product
+// is split into its float value and its exact error by an fma, and the warp
+// butterfly adds the values with an error-free two-sum, carrying the errors
+// beside them. The result stays within a few float roundings of the exact dot
+// even when it nearly cancels. Warp sums go to part[warp]; dot128_comp_finish
+// adds the four in a fixed order. The output term of the record a token
+// appends uses it: after a zero state that term is the whole output.
+__device__ __forceinline__ void two_sum_into(float& s, float& c, float o, float oc) {
+  const float t = __fadd_rn(s, o);
+  const float z = __fsub_rn(t, s);
+  const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(o, z));  // s + o - t, exactly
+  c = __fadd_rn(__fadd_rn(c, oc), e);
+  s = t;
+}
+__device__ __forceinline__ void dot128_comp_warp(float x, float y, float2* part) {
+  float s = __fmul_rn(x, y);
+  float c = __fmaf_rn(x, y, -s);  // x y - s, exactly
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, s, off);
+    const float oc = __shfl_xor_sync(0xffffffffu, c, off);
+    two_sum_into(s, c, o, oc);  // exact sums are symmetric: every lane ends with the same pair
+  }
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = make_float2(s, c);
+}
+__device__ __forceinline__ float dot128_comp_finish(const float2* part) {
+  float s0 = part[0].x, c0 = part[0].y, s2 = part[2].x, c2 = part[2].y;
+  two_sum_into(s0, c0, part[1].x, part[1].y);
+  two_sum_into(s2, c2, part[3].x, part[3].y);
+  two_sum_into(s0, c0, s2, c2);
+  return __fadd_rn(s0, c0);
+}
+
 // The same tree over 8 partials held in memory.
 __device__ __forceinline__ float tree8_mem(const float* a, int stride) {
   return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[stride]), __fadd_rn(a[2 * stride], a[3 * stride])),
@@ -526,6 +561,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
   const float* lam = at<float>(sm, L.lambda);
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
+  __shared__ float2 kq_part[4];
 
   // A0: decay products P_n = 1, P_{m-1} = P_m * alpha_m (backward running
   // products over records 1..n-1 and this token's alpha). KDA: thread j runs
@@ -596,17 +632,17 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
     qn_b[jb] = tk.q;
     zk_b[jb] = __fmul_rn(lam[j], yy);
     zq_b[jb] = __fmul_rn(lam[j], qa);
+    dot128_comp_warp(tk.k, tk.q, kq_part);  // k_n . q_n, the new record's output term (P_n = 1)
   }
   __syncthreads();
 
   // A3/A4 reads, one lane group per dot product: records m = 1..n-1, then the
-  // compensators, then k_n . q_n (the new record's output term, P_n = 1).
-  // The k-side sums (g, ec) are pinned; the q-side (h, eq) only feeds o.
-  // Record m's sums sit at g[m-1], h[m-1]; k_n . q_n at h[n-1].
+  // compensators. The k-side sums (g, ec) are pinned; the q-side (h, eq) only
+  // feeds o. Record m's sums sit at g[m-1], h[m-1].
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
-    const int njobs = nrec + p.C + 1;
+    const int njobs = nrec + p.C;
     for (int base = 0; base < njobs; base += NG) {
       const int job = base + grp;
       float pa = 0.0f, pb = 0.0f;
@@ -648,7 +684,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
               }
             }
           }
-        } else if (job < nrec + p.C) {
+        } else {
           // y = A_n . k_n and A_n . q_n, formed again from the blocked k and q
           const int c = job - nrec;
           const int id = cid[c];
@@ -678,17 +714,6 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
               pb = __fmaf_rn(bs[e], __fmul_rn(av[e], qxs[e]), pb);
             }
           }
-        } else {
-          const float4* kx4 = reinterpret_cast<const float4*>(kn_b + 20 * qq);
-          const float4* qx4 = reinterpret_cast<const float4*>(qn_b + 20 * qq);
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 kx = kx4[c4], qx = qx4[c4];
-            pb = __fmaf_rn(kx.x, qx.x, pb);
-            pb = __fmaf_rn(kx.y, qx.y, pb);
-            pb = __fmaf_rn(kx.z, qx.z, pb);
-            pb = __fmaf_rn(kx.w, qx.w, pb);
-          }
         }
       }
       pa = tree8(pa);
@@ -697,11 +722,9 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
         if (job < nrec) {
           g[job] = pa;
           h[job] = KDA ? pb : __fmul_rn(P[job + 1], pb);
-        } else if (job < nrec + p.C) {
+        } else {
           ec[job - nrec] = pa;
           eq[job - nrec] = pb;
-        } else {
-          h[n - 1] = pb;
         }
       }
     }
@@ -792,7 +815,7 @@ __device__ __forceinline__ void append_compute(const Params& p, int64_t s, int n
       }
     }
     const float u = __fmul_rn(beta, __fsub_rn(tk.v, acc));
-    oo = __fmaf_rn(u, h[n - 1], oo);
+    oo = __fmaf_rn(u, dot128_comp_finish(kq_part), oo);
     p.rec_u[rec_off + i] = u;
     p.o[s * kD + i] = oo;
     p.rec_k[rec_off + i] = tk.k;
@@ -841,6 +864,7 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
   const float* lam = at<float>(sm, L.lambda);
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
+  __shared__ float2 er_part[4], kr_part[4];
 
   // A0: both product chains of column j.
   if (tid < kD) {
@@ -875,20 +899,22 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
     const int j = tid, jb = bv(j);
     kn_b[jb] = tk.k;
     khn_b[jb] = khv;
-    en_b[jb] = __fmul_rn(kav, khv);
+    const float en = __fmul_rn(kav, khv);
+    en_b[jb] = en;
     qn_b[jb] = tk.q;
     zk_b[jb] = __fmul_rn(lam[j], __fmul_rn(Pp_b[jb], khv));
     zq_b[jb] = __fmul_rn(lam[j], __fmul_rn(P_b[jb], tk.q));
+    dot128_comp_warp(en, tk.q, er_part);  // the erase key against r (P_n = 1)
+    dot128_comp_warp(tk.k, tk.q, kr_part);  // k . r
   }
   __syncthreads();
 
   // Dot products, one lane group each: records m = 1..n-1 against kh (read,
-  // with P'_m) and r (output, with P_m); the compensators against both; the
-  // erase key against r (P_n = 1); k . r.
+  // with P'_m) and r (output, with P_m); the compensators against both.
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
-    const int njobs = nrec + p.C + 2;
+    const int njobs = nrec + p.C;
     for (int base = 0; base < njobs; base += NG) {
       const int job = base + grp;
       float pa = 0.0f, pb = 0.0f;
@@ -920,7 +946,7 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
               pb = __fmaf_rn(kvs[e], __fmul_rn(pms[e], qxs[e]), pb);
             }
           }
-        } else if (job < nrec + p.C) {
+        } else {
           const int c = job - nrec;
           const int id = cid[c];
           const float4* b4 = reinterpret_cast<const float4*>(cl + (FIT ? (2 * c + 1) * kD : c * kD) + 16 * qq);
@@ -939,17 +965,6 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
               pb = __fmaf_rn(bs[e], __fmul_rn(a0s[e], qxs[e]), pb);
             }
           }
-        } else {
-          // the erase key (record n, P_n = 1) or the write key (record n+1) against r
-          const float4* x4 = reinterpret_cast<const float4*>((job == nrec + p.C ? en_b : kn_b) + 20 * qq);
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 x = x4[c4], qx = qx4[c4];
-            pb = __fmaf_rn(x.x, qx.x, pb);
-            pb = __fmaf_rn(x.y, qx.y, pb);
-            pb = __fmaf_rn(x.z, qx.z, pb);
-            pb = __fmaf_rn(x.w, qx.w, pb);
-          }
         }
       }
       pa = tree8(pa);
@@ -958,11 +973,9 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
         if (job < nrec) {
           g[job] = pa;
           h[job] = pb;
-        } else if (job < nrec + p.C) {
+        } else {
           ec[job - nrec] = pa;
           eq[job - nrec] = pb;
-        } else {
-          h[job - p.C] = pb;  // h[n-1]: the erase key, h[n]: the write key
         }
       }
     }
@@ -1045,8 +1058,8 @@ __device__ __forceinline__ void append_rwkv_compute(const Params& p, int64_t s, 
       }
     }
     const float ue = -acc;
-    oo = __fmaf_rn(ue, h[n - 1], oo);
-    oo = __fmaf_rn(tk.v, h[n], oo);
+    oo = __fmaf_rn(ue, dot128_comp_finish(er_part), oo);
+    oo = __fmaf_rn(tk.v, dot128_comp_finish(kr_part), oo);
     p.rec_u[rec_off + i] = ue;
     p.rec_u[rec_off + kD + i] = tk.v;
     p.rec_k[rec_off + i] = en_b[bv(i)];
@@ -1096,6 +1109,7 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
   const float* lam = at<float>(sm, L.lambda);
   const int32_t* cid = at<int32_t>(sm, L.comp_id);
   const float* cl = at<float>(sm, L.comp_line);
+  __shared__ float2 k1q_part[4], k2q_part[4];
 
   // A0: the decay products of record n's append (P_n = 1, P_{m-1} = P_m alpha_m);
   // record n+1 adds P_{n+1} = 1 and leaves the rest unchanged.
@@ -1153,15 +1167,17 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
     zk_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, tk.k));
     zk2_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, k2v));
     zq_b[jb] = __fmul_rn(lam[j], __fmul_rn(A, tk.q));
+    dot128_comp_warp(tk.k, tk.q, k1q_part);  // record n against q (P_n = 1)
+    dot128_comp_warp(k2v, tk.q, k2q_part);   // k2 . q
   }
   __syncthreads();
 
   // Dot products, one lane group each: records m = 1..n-1 against k1, k2 and q;
-  // the compensators against the three; record n (k1) against k2 and q; k2 . q.
+  // the compensators against the three; record n (k1) against k2.
   {
     const int grp = tid >> 3;
     const int nrec = n - 1;
-    const int njobs = nrec + p.C + 2;
+    const int njobs = nrec + p.C + 1;
     for (int base = 0; base < njobs; base += NG) {
       const int job = base + grp;
       float pa = 0.0f, pa2 = 0.0f, pb = 0.0f;
@@ -1237,15 +1253,6 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
               pb = __fmaf_rn(bs[e], __fmul_rn(av[e], qxs[e]), pb);
             }
           }
-        } else {
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 k2x = k2x4[c4], qx = qx4[c4];
-            pb = __fmaf_rn(k2x.x, qx.x, pb);
-            pb = __fmaf_rn(k2x.y, qx.y, pb);
-            pb = __fmaf_rn(k2x.z, qx.z, pb);
-            pb = __fmaf_rn(k2x.w, qx.w, pb);
-          }
         }
       }
       pa = tree8(pa);
@@ -1260,11 +1267,8 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
           ec[job - nrec] = pa;
           ec2[job - nrec] = pa2;
           eq[job - nrec] = pb;
-        } else if (job == nrec + p.C) {
-          g2[n - 1] = pa2;
-          h[n - 1] = KDA ? pb : __fmul_rn(P[n], pb);
         } else {
-          h[n] = pb;
+          g2[n - 1] = pa2;
         }
       }
     }
@@ -1359,9 +1363,9 @@ __device__ __forceinline__ void append2_compute(const Params& p, int64_t s, int 
     }
     const float u1 = __fmul_rn(beta1, __fsub_rn(tk.v, acc));
     acc2 = __fmaf_rn(u1, g2[n - 1], acc2);
-    oo = __fmaf_rn(u1, h[n - 1], oo);
+    oo = __fmaf_rn(u1, dot128_comp_finish(k1q_part), oo);
     const float u2 = __fmul_rn(beta2, __fsub_rn(v2v, acc2));
-    oo = __fmaf_rn(u2, h[n], oo);
+    oo = __fmaf_rn(u2, dot128_comp_finish(k2q_part), oo);
     p.rec_u[rec_off + i] = u1;
     p.rec_u[rec_off + kD + i] = u2;
     p.rec_k[rec_off + i] = tk.k;
