@@ -163,7 +163,10 @@ int lq_state_init_range(const lq_config* cfg, void* state, int64_t n_states, int
  * unchanged and the status word is set to LQ_ERR_WINDOW_FULL.
  *   q, k  fp32 [n_states][d_k];  v, o  fp32 [n_states][d_v]
  *   alpha fp32 [n_states] (GDN) or [n_states][d_k] (KDA);  beta fp32 [n_states]
- * o may not alias any input.
+ * o may not alias any input. o's summation order is free; its term for the
+ * new record, u (k . q), uses a compensated dot, so it stays within a few
+ * float roundings of exact even when k . q nearly cancels (after a zero
+ * state it is the whole output).
  */
 int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k, const float* v,
               const float* alpha, const float* beta, float* o, lq_stream_t stream);
