@@ -102,6 +102,11 @@ def compare_boundary(g, ref: OracleState, ref_idx, diags=None, tally: Tally | No
     ref_idx = list(ref_idx)
     assert np.array_equal(g["count"], ref.count[ref_idx]), what
     assert np.array_equal(g["comp_id"][:, :C], ref.comp_id[ref_idx, :C]), (what, g["comp_id"], ref.comp_id[ref_idx])
+    # sigma, lambda and the compensator lines do not depend on how a tie rounds:
+    # they are compared on every fold, whatever the codes do
+    assert np.array_equal(g["sigma"], ref.sigma[ref_idx]), what
+    assert np.array_equal(g["lam"], ref.lam[ref_idx]), what
+    assert np.array_equal(g["comp_line"][:, :C], ref.comp_line[ref_idx, :C]), what
     codes_r = ref.codes[ref_idx]
     diff = g["codes"] != codes_r
     n = int(diff.sum())
@@ -115,9 +120,6 @@ def compare_boundary(g, ref: OracleState, ref_idx, diags=None, tally: Tally | No
         if tally is not None:
             tally.mismatch += n
         return n
-    assert np.array_equal(g["sigma"], ref.sigma[ref_idx]), what
-    assert np.array_equal(g["lam"], ref.lam[ref_idx]), what
-    assert np.array_equal(g["comp_line"][:, :C], ref.comp_line[ref_idx, :C]), what
     return 0
 
 

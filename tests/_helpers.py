@@ -49,3 +49,23 @@ def read_golden(name):
             k, v = (x.strip() for x in line.split("=", 1))
             out[k] = float(v) if "." in v else int(v)
     return out
+
+
+def tie_rows(qm):
+    """Rows whose t * h values are exact half-integers (C = 0, smoothing off, so t = R and
+    h = qm / max|row|) and the codes round-half-to-even gives them, typed out by hand.
+    Row r is the base row times 2^(r - 1), so h = 2^(1 - r) exactly and every product
+    stays a half-integer."""
+    base = [qm, 0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, -3.5, qm - 0.5, -(qm - 0.5), 4.5, -4.5]
+    if qm == 7:
+        want = [7, 0, 2, 2, 4, 0, -2, -2, -4, 6, -6, 4, -4]
+    elif qm == 31:
+        want = [31, 0, 2, 2, 4, 0, -2, -2, -4, 30, -30, 4, -4]
+    else:
+        want = [127, 0, 2, 2, 4, 0, -2, -2, -4, 126, -126, 4, -4]
+    S0 = np.zeros((1, 128, 128), np.float32)
+    codes = np.zeros((1, 128, 128), np.int8)
+    for r in range(3):
+        S0[0, r, :len(base)] = np.float32(2.0 ** (r - 1)) * np.asarray(base, np.float32)
+        codes[0, r, :len(want)] = want
+    return S0, codes

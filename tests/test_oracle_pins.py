@@ -19,7 +19,7 @@ import pytest
 import oracle
 from oracle import FoldDiag, OracleState
 from quantized_linear_attention_gb300 import workload as wlm
-from tests._helpers import code_mismatches, near_tie, rel_l2
+from tests._helpers import code_mismatches, near_tie, rel_l2, tie_rows
 
 
 # ---------------------------------------------------------------- dot products
@@ -422,3 +422,20 @@ def test_window_full_is_an_error():
     st.run(x, x, x, one, one, fold_when_full=False)
     with pytest.raises(RuntimeError):
         st.run(x, x, x, one, one, fold_when_full=False)
+
+
+# ---------------------------------------------------------------- F5 at exact ties
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_f5_rounds_exact_ties_to_even(bits):
+    """Reading R8 (the pages leave the rounding mode open: research note 4, "Why rounding
+    the state is difficult"): F5 rounds half to even. Half away from zero, truncation or
+    rounding half up all miss at least one of these typed-out codes."""
+    qm = 2 ** (bits - 1) - 1
+    S0, want = tie_rows(qm)
+    st = OracleState(1, C=0, smooth=False, code_bits=bits)
+    dg = [FoldDiag(128, 128)]
+    st.init(S0, diags=dg)
+    # the values handed to the rounding are the exact half-integers themselves
+    assert np.array_equal(dg[0].s_round[:3, :13] * 2, np.rint(dg[0].s_round[:3, :13] * 2))
+    assert np.array_equal(st.codes, want)
+    assert np.array_equal(st.sigma[0, :3], (np.float32(qm) * np.float32([0.5, 1.0, 2.0])) / np.float32(qm))

@@ -4,8 +4,11 @@ From a zero state the first token's output is the new record's term alone,
 o = u (k . q) with u = beta v (LeapQuant §3.1: the state after one delta-rule
 step is beta v k^T). When q is nearly orthogonal to k, k . q is a small
 difference of large products and a float32 sum of the 128 products loses most
-of its digits. The kernels form that term from exact products summed in
-double, so the output stays within float rounding of the exact value. The
+of its digits. The kernels form that term as a compensated float dot (each
+product split into its float value and exact error, the values added with
+error-free two-sums and the errors carried beside them): the result is as if
+summed in twice the float precision and rounded once, so the output stays
+within a few float roundings of the exact value. The
 cases cover one-record tokens (scalar and per-key decay), two-record tokens
 (q nearly orthogonal to both keys) and RWKV7 tokens (r nearly orthogonal to
 the write key; the erase record is empty at a zero state).

@@ -65,3 +65,22 @@ def test_separate_append_and_fold_match_fused_step():
 
     wl = wlm.custom(400, 11, 0, n_warm=40, plant=True)
     run_and_compare(wl, 2 * 16 + 4, use_append_fold=True)
+
+
+@pytest.mark.parametrize("bits", [8, 6, 4])
+def test_exact_ties_round_to_even(bits):
+    """The init-fold's rounding at exact half-integers (reading R8: half to even), the
+    same typed-out codes the oracle is pinned to; then a fold with no records keeps them."""
+    from tests._gpu import GpuState, to_dev
+    from tests._helpers import tie_rows
+
+    qm = 2 ** (bits - 1) - 1
+    S0, want = tie_rows(qm)
+    g = GpuState(1, C=0, smooth=False, code_bits=bits)
+    g.init(S0)
+    b = g.boundary()
+    assert np.array_equal(b["codes"], want)
+    assert np.array_equal(b["sigma"][0, :3], (np.float32(qm) * np.float32([0.5, 1.0, 2.0])) / np.float32(qm))
+    g.fold()
+    assert np.array_equal(g.boundary()["codes"], want)
+    assert g.status()[0] == lq.OK
