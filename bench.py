@@ -208,6 +208,24 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- our arm
+def run_config(wl, world):
+    """The config object both arms print (the reference arm times the same workload)."""
+    return dict(workload_config(wl, 4 * wl.W),
+                parallelism=f"dp{world}: {wl.n_states} head-states per rank, disjoint request blocks, no collective")
+
+
+def host_cpu_model():
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.uname().machine
+
+
 def workload_config(wl, pool_tokens):
     return {"workload": wl.name, "n_states": wl.n_states, "batch": wl.requests, "layers": wl.layers,
             "heads": wl.heads, "d_k": wl.dk, "d_v": wl.dv, "W": wl.W, "C": wl.C,
@@ -623,22 +641,27 @@ def cpu_baseline(wl, budget_s=12.0):
     cores = os.cpu_count() or 1
     W = wl.W
 
-    def run(M):
+    def run(M, threads):
         S0, _ = wlm.initial_state(wl, 0, M)
         tk = wlm.tokens(wl, 0, W, 0, M)
         st = oracle.OracleState(M, W=W, C=wl.C, decay_per_key=wl.kda)
         st.init(S0)
         t0 = time.perf_counter()
-        st.run(tk.q, tk.k, tk.v, tk.alpha, tk.beta, nthreads=cores, want_o=True)
+        st.run(tk.q, tk.k, tk.v, tk.alpha, tk.beta, nthreads=threads, want_o=True)
         return time.perf_counter() - t0
 
     m0 = min(wl.n_states, max(cores, 32))
-    rate = m0 * W / run(m0)
+    rate = m0 * W / run(m0, cores)
     M = int(min(wl.n_states, max(m0, rate * budget_s / W)))
-    dt = run(M)
+    dt = run(M, cores)
+    m1 = min(wl.n_states, 16)
+    rate1 = m1 * W / run(m1, 1)
+    M1 = int(min(wl.n_states, max(m1, rate1 * budget_s / 3 / W)))
+    dt1 = run(M1, 1)
     return {"value": round(M * W / dt, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{M} of {wl.n_states} head-states x {W} tokens (one window, fold included) of {wl.name}; "
-                      f"{dt:.1f} s on {cores} threads ({os.uname().machine})"}
+            "single_core": round(M1 * W / dt1, 1), "host_cpu": f"{host_cpu_model()} ({os.uname().machine})",
+            "sample": f"{M} (1 core: {M1}) of {wl.n_states} head-states x {W} tokens (one window, fold included) "
+                      f"of {wl.name}; {dt:.1f} s on {cores} threads, {dt1:.1f} s on 1"}
 
 
 def run_ours(args):
@@ -679,7 +702,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(t_ms / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(wl, 4 * W), parallelism=f"dp{world}: {N} head-states per rank, disjoint request blocks, no collective"),
+        "config": run_config(wl, world),
         "roofline": {"bound": "hbm", "kernel": "k_append (append-only decode step, phases 0..14)",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs (copy)",
@@ -708,8 +731,7 @@ def run_ours(args):
             sweep[f"batch{swl.requests}"] = {
                 "head_tokens_per_s": round(swl.n_states * swl.W * args.sweep_steps / (total / 1e3), 1),
                 "append_step_us": round(a_ms * 1e3, 2), "fold_step_us": round(f_ms * 1e3, 2),
-                "window_gbs": round(gbs, 1), "window_frac": round(gbs / hbm, 4),
-                "note": "CUDA-graph replays; the working set may sit in L2 (effective bandwidth)"}
+                "window_gbs": round(gbs, 1), "window_frac": round(gbs / hbm, 4), "note": "graph; L2 may hold it"}
         sweep[f"batch{wl.requests}"] = {
             "head_tokens_per_s": round(value / world, 1), "append_step_us": round(app_ms * 1e3, 2),
             "fold_step_us": round(fold_ms * 1e3, 2), "window_gbs": round(win_gbs, 1),
@@ -816,7 +838,12 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
-        print(json.dumps(result), flush=True)
+        # the summaries the metric names (batches 32/128/512, the fold step, the
+        # window) and the baselines go last, where a truncated tail still shows them
+        last = ("window", "fold_step", "batches", "e2e", "cpu_baseline", "gpu_launches", "clocks")
+        ordered = {k: v for k, v in result.items() if k not in last}
+        ordered.update((k, result[k]) for k in last if k in result)
+        print(json.dumps(ordered), flush=True)
     if world > 1:
         import torch.distributed as dist
 
@@ -867,9 +894,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(wl, 2 * W), parallelism="host cores (oracle)"),
+        "config": run_config(wl, world),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "host_cpu": f"{host_cpu_model()} ({os.uname().machine})", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -37,7 +37,8 @@
  *     the device (a full window, a phase mismatch, a state buffer written with
  *     another configuration) set the state buffer's status word, which
  *     lq_get_status reads; the affected head-states are left unchanged.
- *   - Threads: no global mutable state except a thread-local error message.
+ *   - Threads: no global mutable state except a thread-local error message,
+ *     and the thread-local test hook of lq_debug_set_wait.
  *   - n_states = 0 is valid and does nothing.
  */
 #ifndef LQ_H
@@ -79,7 +80,8 @@ typedef struct {
   int32_t comp_fit;      /* 0 (default): a compensator is an outlier line, kept exactly;     */
                          /* 1..32: a rank-one factor a b^T fitted to the residual by that   */
                          /* many power-iteration sweeps from the longest row ([LQ] §3.3,    */
-                         /* App. B.3 "fitting new factors"; [RN4] "Where the time goes")    */
+                         /* App. B.3, new factors fitted at the boundary; [RN4] "Where the */
+                         /* time goes")                                                      */
   int32_t comp_block;    /* with comp_fit > 0: 1 fits the C factors together as a block     */
                          /* (subspace iteration), each fold starting from the previous      */
                          /* window's factors ([RN4] "Redesign"); 0 (default) one at a time  */
@@ -128,17 +130,32 @@ typedef struct {
 /* Default configuration: d_k = d_v = 128, W = 16, C = 4, GDN, smoothing on, floor 1e-6, 8-bit codes. */
 void lq_config_default(lq_config* cfg);
 
-/* Bytes the caller must allocate for n_states head-states (0 if cfg or n_states is invalid). */
+/*
+ * Bytes the caller must allocate for n_states head-states (0 if cfg or n_states
+ * is invalid): the boundary of each head-state (LeapQuant summary §3.2
+ * Per-window quantization: codes with their row steps; §3.3 Compensator Tokens;
+ * §3.4 Residual smoothing; §4.3 Efficiency results gives 1.19 bytes per element
+ * for it) plus its window's record buffer (research note 4, "What we built":
+ * each token's change is kept as a record until the fold). Host only.
+ */
 size_t lq_state_bytes(const lq_config* cfg, int64_t n_states);
 
-/* Fill *out with the plane offsets for n_states head-states. Host only; never touches a GPU. */
+/* Fill *out with the plane offsets for n_states head-states (the planes listed above:
+ * LeapQuant summary §3.2-3.4 for the boundary, research note 4 "What we built" for the
+ * records). Host only; never touches a GPU. Errors: LQ_ERR_INVALID_ARG (NULL out, bad
+ * n_states), LQ_ERR_UNSUPPORTED (a configuration this build does not run). */
 int lq_layout(const lq_config* cfg, int64_t n_states, lq_layout_t* out);
 
 /*
  * Initialise a state buffer: write the header, set every record count to 0 and
- * init-fold S0 into the boundary (compensator selection, smoothing, rounding;
- * the fold of §3.3-3.4 without records). S0 is fp32 [n_states][d_v][d_k], or
- * NULL for the zero state. Clears the status word.
+ * init-fold S0 into the boundary. This is the fold with no records: compensator
+ * selection (LeapQuant summary §3.3 Compensator Tokens), smoothing (§3.4
+ * Residual smoothing) and one rounding per row step (§3.2 Per-window
+ * quantization; research note 4, "Why rounding the state is difficult").
+ * S0 is fp32 [n_states][d_v][d_k] (row i = value channel), or NULL for the
+ * zero state; it is only read. Clears the status word. Errors:
+ * LQ_ERR_INVALID_ARG for a NULL or misaligned pointer (state 256 bytes, S0 16
+ * bytes), memory not on the current device, or bad n_states.
  */
 int lq_state_init(const lq_config* cfg, void* state, int64_t n_states, const float* S0, lq_stream_t stream);
 
@@ -171,7 +188,16 @@ int lq_state_init_range(const lq_config* cfg, void* state, int64_t n_states, int
 int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k, const float* v,
               const float* alpha, const float* beta, float* o, lq_stream_t stream);
 
-/* Fold every head-state with the records it holds (any count 0..W), then empty the buffer. */
+/*
+ * Fold every head-state with the records it holds (any count 0..W), then empty
+ * the buffer: rebuild the state in original coordinates from the boundary and
+ * the records (LeapQuant summary App. B.3: reconstructed before fitting new
+ * factors), select the compensators (§3.3), smooth the residual (§3.4) and
+ * round it once (§3.2); research note 4, "What we built", names this second
+ * part of the kernel, which also empties the record buffer.
+ * A head-state whose header or record count is invalid is left unchanged and
+ * sets LQ_ERR_STATE in the status word.
+ */
 int lq_fold(const lq_config* cfg, void* state, int64_t n_states, lq_stream_t stream);
 
 /*
@@ -236,7 +262,10 @@ int lq_decode_step_rwkv7(const lq_config* cfg, void* state, int64_t n_states, in
 /*
  * Write the state each head-state stands for, S_n = boundary x Diag(A_n) plus
  * the buffered records, in original coordinates (the fold's reconstruction,
- * without rounding), to S_out fp32 [n_states][d_v][d_k]. The state is unchanged.
+ * without rounding: LeapQuant summary App. B.2 window unrolling, App. B.3
+ * reconstruction in original coordinates), to S_out fp32 [n_states][d_v][d_k],
+ * caller-owned, 16-byte aligned, not overlapping the state buffer. The state
+ * is unchanged.
  */
 int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, float* S_out, lq_stream_t stream);
 
@@ -270,6 +299,29 @@ const char* lq_last_error(void);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int lq_version(void);
+
+/*
+ * Test hook for the kernels' failure path; not for production use. Every
+ * wait inside a kernel (for the bulk copies that stage a head-state into
+ * shared memory) is bounded; when the bound runs out the kernel records
+ * LQ_ERR_TIMEOUT in the status word with the head-state's index, leaves that
+ * head-state unchanged and returns, so the context stays usable. After
+ * LQ_ERR_TIMEOUT treat every output of that call as untrusted (copies may
+ * still have been landing in the shared memory of the CTA that gave up) and
+ * re-initialise the state before going on.
+ * This call sets, for later calls made by this thread only:
+ *   wait_ns          the bound on each wait (1..1e9 ns; 0 restores the 1 s default);
+ *   extra_tx_append  bytes the append kernels (lq_append, lq_decode_step below
+ *                    the window's last token, the two-record and RWKV7 steps)
+ *                    announce to their barrier beyond those they copy (0..1024);
+ *   extra_tx_fold    the same for the kernels that stage the records (the fused
+ *                    last token of a window, lq_fold, the list fold, lq_export_state).
+ * With an extra byte count the copies all land and the barrier never completes,
+ * so the wait runs out after wait_ns. lq_state_init has no such wait (it reads
+ * S0 with plain loads). The pages have no counterpart; the failure-detection
+ * design is this library's. Errors: LQ_ERR_INVALID_ARG for values out of range.
+ */
+int lq_debug_set_wait(uint64_t wait_ns, int32_t extra_tx_append, int32_t extra_tx_fold);
 
 #ifdef __cplusplus
 }

@@ -21,6 +21,12 @@ namespace {
 
 thread_local char g_err[512] = "";
 
+// Test hook (lq_debug_set_wait): this thread's bound on kernel waits and the
+// bytes the append / fold kernels announce beyond those they copy.
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
+thread_local uint64_t g_wait_ns = kWaitNs;
+thread_local int32_t g_tx_append = 0, g_tx_fold = 0;
+
 int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -147,9 +153,16 @@ int check_stream(lq_stream_t stream, int dev) {
   return LQ_OK;
 }
 
-int check_ptr(const void* p, const char* name, size_t align, int dev) {
+// Host-only part of a pointer check: not NULL, aligned.
+int check_addr(const void* p, const char* name, size_t align) {
   if (!p) return fail(LQ_ERR_INVALID_ARG, "%s is NULL", name);
   if ((uintptr_t)p % align != 0) return fail(LQ_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+  return LQ_OK;
+}
+
+int check_ptr(const void* p, const char* name, size_t align, int dev) {
+  int rc = check_addr(p, name, align);
+  if (rc) return rc;
   cudaPointerAttributes a;
   cudaError_t e = cudaPointerGetAttributes(&a, p);
   if (e != cudaSuccess) {
@@ -183,6 +196,9 @@ Params make_params(const lq_config* c, void* state, int64_t n) {
   p.comp_block = c->comp_block;
   p.lambda_floor = c->lambda_floor;
   p.phase = -1;
+  p.wait_ns = g_wait_ns;
+  p.dbg_tx_append = g_tx_append;
+  p.dbg_tx_fold = g_tx_fold;
   p.n_states = n;
   p.cfg_hash = cfg_hash(c, n);
   p.comp_id_stride = L.comp_id_stride;
@@ -202,30 +218,62 @@ Params make_params(const lq_config* c, void* state, int64_t n) {
 }
 
 // Common validation of (cfg, state, n, stream); *dev receives the current device.
+// The checks that need no GPU (configuration, size, alignment) come first.
 int check_common(const lq_config* cfg, const void* state, int64_t n, lq_stream_t stream, int* dev) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if ((rc = check_n(n))) return rc;
   if (n == 0) return LQ_OK;
+  if ((rc = check_addr(state, "state", 256))) return rc;
   if ((rc = current_device(dev))) return rc;
   if ((rc = check_stream(stream, *dev))) return rc;
   return check_ptr(state, "state", 256, *dev);
 }
 
-int check_tokens(const lq_config* cfg, int64_t n, int dev, const float* q, const float* k, const float* v,
-                 const float* alpha, const float* beta, const float* o) {
+// Bytes of the state buffer of (cfg, n): an output must not overlap it.
+size_t state_size(const lq_config* cfg, int64_t n) {
+  lq_layout_t L;
+  make_layout(cfg, n, &L);
+  return L.total_bytes;
+}
+
+// Host-only checks of a token's inputs and output o: NULL, alignment, and o
+// overlapping an input or the state buffer (which the same kernels read and write).
+int check_tokens_host(const lq_config* cfg, int64_t n, const void* state, const float* q, const float* k,
+                      const float* v, const float* alpha, const float* beta, const float* o) {
   int rc;
-  if ((rc = check_ptr(q, "q", 16, dev)) || (rc = check_ptr(k, "k", 16, dev)) || (rc = check_ptr(v, "v", 16, dev)) ||
-      (rc = check_ptr(alpha, "alpha", 4, dev)) || (rc = check_ptr(beta, "beta", 4, dev)) ||
-      (rc = check_ptr(o, "o", 16, dev)))
+  if ((rc = check_addr(q, "q", 16)) || (rc = check_addr(k, "k", 16)) || (rc = check_addr(v, "v", 16)) ||
+      (rc = check_addr(alpha, "alpha", cfg->decay_per_key ? 16 : 4)) || (rc = check_addr(beta, "beta", 4)) ||
+      (rc = check_addr(o, "o", 16)))
     return rc;
-  if (cfg->decay_per_key && (uintptr_t)alpha % 16 != 0)
-    return fail(LQ_ERR_INVALID_ARG, "alpha (per key channel) is not 16-byte aligned");
   const size_t vec = (size_t)n * kD * sizeof(float);
   const size_t na = cfg->decay_per_key ? vec : (size_t)n * sizeof(float);
   if (overlaps(o, vec, q, vec) || overlaps(o, vec, k, vec) || overlaps(o, vec, v, vec) ||
       overlaps(o, vec, alpha, na) || overlaps(o, vec, beta, (size_t)n * sizeof(float)))
     return fail(LQ_ERR_INVALID_ARG, "o overlaps an input");
+  if (state && overlaps(o, vec, state, state_size(cfg, n)))
+    return fail(LQ_ERR_INVALID_ARG, "o overlaps the state buffer");
+  return LQ_OK;
+}
+
+// The host-only checks of a token call, before anything asks the GPU.
+int precheck_tokens(const lq_config* cfg, const void* state, int64_t n, const float* q, const float* k,
+                    const float* v, const float* alpha, const float* beta, const float* o) {
+  int rc = check_cfg(cfg);
+  if (rc || (rc = check_n(n))) return rc;
+  if (n == 0) return LQ_OK;
+  if ((rc = check_addr(state, "state", 256))) return rc;
+  return check_tokens_host(cfg, n, state, q, k, v, alpha, beta, o);
+}
+
+int check_tokens(const lq_config* cfg, int64_t n, int dev, const float* q, const float* k, const float* v,
+                 const float* alpha, const float* beta, const float* o, const void* state = nullptr) {
+  int rc = check_tokens_host(cfg, n, state, q, k, v, alpha, beta, o);
+  if (rc) return rc;
+  if ((rc = check_ptr(q, "q", 16, dev)) || (rc = check_ptr(k, "k", 16, dev)) || (rc = check_ptr(v, "v", 16, dev)) ||
+      (rc = check_ptr(alpha, "alpha", 4, dev)) || (rc = check_ptr(beta, "beta", 4, dev)) ||
+      (rc = check_ptr(o, "o", 16, dev)))
+    return rc;
   return LQ_OK;
 }
 
@@ -238,6 +286,16 @@ extern "C" {
 const char* lq_last_error(void) { return g_err; }
 
 int lq_version(void) { return 100; }
+
+int lq_debug_set_wait(uint64_t wait_ns, int32_t extra_tx_append, int32_t extra_tx_fold) {
+  if (wait_ns > kWaitNs) return fail(LQ_ERR_INVALID_ARG, "wait_ns must be 0..%llu", (unsigned long long)kWaitNs);
+  if (extra_tx_append < 0 || extra_tx_append > 1024 || extra_tx_fold < 0 || extra_tx_fold > 1024)
+    return fail(LQ_ERR_INVALID_ARG, "extra_tx bytes must be 0..1024");
+  g_wait_ns = wait_ns ? wait_ns : kWaitNs;
+  g_tx_append = extra_tx_append;
+  g_tx_fold = extra_tx_fold;
+  return ok();
+}
 
 void lq_config_default(lq_config* cfg) {
   if (!cfg) return;
@@ -300,9 +358,9 @@ int lq_state_init_range(const lq_config* cfg, void* state, int64_t n_states, int
 int lq_append(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k, const float* v,
               const float* alpha, const float* beta, float* o, lq_stream_t stream) {
   int dev = 0;
-  int rc = check_common(cfg, state, n_states, stream, &dev);
-  if (rc || n_states == 0) return rc ? rc : ok();
-  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o))) return rc;
+  int rc = precheck_tokens(cfg, state, n_states, q, k, v, alpha, beta, o);
+  if (rc || (rc = check_common(cfg, state, n_states, stream, &dev)) || n_states == 0) return rc ? rc : ok();
+  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o, state))) return rc;
   Params p = make_params(cfg, state, n_states);
   p.q = q;
   p.k = k;
@@ -325,12 +383,12 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
                    const float* k, const float* v, const float* alpha, const float* beta, float* o,
                    lq_stream_t stream) {
   int dev = 0;
-  int rc = check_common(cfg, state, n_states, stream, &dev);
-  if (rc) return rc;
+  int rc = precheck_tokens(cfg, state, n_states, q, k, v, alpha, beta, o);
+  if (rc || (rc = check_common(cfg, state, n_states, stream, &dev))) return rc;
   if (phase != LQ_PHASE_ANY && (phase < 0 || phase >= cfg->window))
     return fail(LQ_ERR_INVALID_ARG, "phase must be LQ_PHASE_ANY or 0..W-1 (got %d)", phase);
   if (n_states == 0) return ok();
-  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o))) return rc;
+  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o, state))) return rc;
   Params p = make_params(cfg, state, n_states);
   p.q = q;
   p.k = k;
@@ -358,13 +416,13 @@ int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t
                     const float* k1, const float* v1, const float* beta1, const float* k2, const float* v2,
                     const float* beta2, const float* alpha, float* o, lq_stream_t stream) {
   int dev = 0;
-  int rc = check_common(cfg, state, n_states, stream, &dev);
-  if (rc) return rc;
+  int rc = precheck_tokens(cfg, state, n_states, q, k1, v1, alpha, beta1, o);
+  if (rc || (rc = check_common(cfg, state, n_states, stream, &dev))) return rc;
   if (cfg->window < 2) return fail(LQ_ERR_UNSUPPORTED, "two-record tokens need a window of at least 2 records");
   if (phase != LQ_PHASE_ANY && (phase < 0 || phase > cfg->window - 2))
     return fail(LQ_ERR_INVALID_ARG, "phase must be LQ_PHASE_ANY or 0..W-2 (got %d)", phase);
   if (n_states == 0) return ok();
-  if ((rc = check_tokens(cfg, n_states, dev, q, k1, v1, alpha, beta1, o))) return rc;
+  if ((rc = check_tokens(cfg, n_states, dev, q, k1, v1, alpha, beta1, o, state))) return rc;
   if ((rc = check_ptr(k2, "k2", 16, dev)) || (rc = check_ptr(v2, "v2", 16, dev)) ||
       (rc = check_ptr(beta2, "beta2", 4, dev)))
     return rc;
@@ -409,6 +467,8 @@ int lq_decode_step_rwkv7(const lq_config* cfg, void* state, int64_t n_states, in
   const size_t vec = (size_t)n_states * kD * sizeof(float);
   for (int t = 0; t < 6; ++t)
     if (overlaps(o, vec, in[t], vec)) return fail(LQ_ERR_INVALID_ARG, "o overlaps an input");
+  if (overlaps(o, vec, state, state_size(cfg, n_states)))
+    return fail(LQ_ERR_INVALID_ARG, "o overlaps the state buffer");
   Params p = make_params(cfg, state, n_states);
   p.q = r;
   p.alpha = w;
@@ -429,6 +489,8 @@ int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, f
   int rc = check_common(cfg, state, n_states, stream, &dev);
   if (rc || n_states == 0) return rc ? rc : ok();
   if ((rc = check_ptr(S_out, "S_out", 16, dev))) return rc;
+  if (overlaps(S_out, (size_t)n_states * kD * kD * sizeof(float), state, state_size(cfg, n_states)))
+    return fail(LQ_ERR_INVALID_ARG, "S_out overlaps the state buffer");
   Params p = make_params(cfg, const_cast<void*>(state), n_states);
   p.S_out = S_out;
   return launched(lqi::launch_export(p, (cudaStream_t)stream), "lq_export_state launch");

@@ -62,6 +62,8 @@ struct Params {
   Header* hdr;
   int32_t* counts;
   int32_t* full_list;
+  uint64_t wait_ns;   // bound on a wait for staged copies (1 s; shorter only under lq_debug_set_wait)
+  int32_t dbg_tx_append, dbg_tx_fold;  // test hook: bytes announced beyond those copied (0 normally)
   int8_t* codes;
   float* sigma;
   float* lambda;

@@ -20,7 +20,7 @@
 // (codes, scales, compensators) and buffered records into shared memory on one
 // mbarrier; the token's inputs and (in the append kernels) the record keys are
 // read straight into registers meanwhile. Global memory sees one burst of
-// reads and the final writes. Waits on the mbarrier are bounded (kWaitNs); on
+// reads and the final writes. Waits on the mbarrier are bounded (1 s); on
 // timeout the kernel records LQ_ERR_TIMEOUT in the state's status word and
 // leaves the head-state unchanged.
 //
@@ -43,7 +43,6 @@
 
 namespace lqi {
 
-constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any wait for copies: 1 s
 
 // ---------------------------------------------------------------------------
 // small device helpers
@@ -318,12 +317,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` for at most kWaitNs; false on timeout.
-__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` for at most limit_ns (1 s unless a test
+// shortened it); false on timeout.
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -441,7 +441,10 @@ __device__ __forceinline__ void stage_issue(const Params& p, int64_t s, int n0, 
   uint32_t bytes = code_bytes + 8u * kD + 4u * (uint32_t)p.comp_id_stride + 4u * comp_floats + rec;
   if (stage_a && (!p.kda || n0 > 0)) bytes += alpha_bytes;
   if (stage_k) bytes += rec;
-  mbar_expect_tx(bar, bytes);
+  // A test can make the barrier expect more bytes than are copied (the append
+  // kernels stage no keys, the fold kernels do): every copy still lands, and
+  // the wait for the rest runs out.
+  mbar_expect_tx(bar, bytes + (uint32_t)(stage_k ? p.dbg_tx_fold : p.dbg_tx_append));
   bulk_g2s(sm + L.codes, p.codes + s * code_bytes, code_bytes, bar);
   bulk_g2s(sm + L.sigma, p.sigma + s * kD, 4 * kD, bar);
   bulk_g2s(sm + L.lambda, p.lambda + s * kD, 4 * kD, bar);
@@ -2316,9 +2319,9 @@ __device__ __forceinline__ int stage_finish(const Params& p, int64_t s, uint64_t
   const int n0 = si.issued, cnt = si.cnt;
   const bool hdr = si.hdr != 0;
   if (n0 >= 0) {
-    const bool ok = mbar_wait_bounded(bar, parity);
+    const bool ok = mbar_wait_bounded(bar, parity, p.wait_ns);
     if (__syncthreads_or(!ok)) {
-      if (!ok) (void)mbar_wait_bounded(bar, parity);  // one more bounded chance for copies in flight
+      if (!ok) (void)mbar_wait_bounded(bar, parity, p.wait_ns);  // one more bounded chance for copies in flight
       if (threadIdx.x == 0) set_error(p, LQ_ERR_TIMEOUT, s);
       return -2;
     }

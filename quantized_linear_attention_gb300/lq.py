@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
 # Every symbol include/lq.h declares.
 EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_state_init_range", "lq_append",
            "lq_fold", "lq_decode_step", "lq_decode_step2", "lq_decode_step_rwkv7", "lq_export_state",
-           "lq_fp32_decode_step", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version")
+           "lq_fp32_decode_step", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version",
+           "lq_debug_set_wait")
 
 
 class Config(ctypes.Structure):
@@ -90,6 +91,7 @@ def load():
         "lq_clear_status": (ctypes.c_int, [P, P]),
         "lq_last_error": (ctypes.c_char_p, []),
         "lq_version": (ctypes.c_int, []),
+        "lq_debug_set_wait": (ctypes.c_int, [ctypes.c_uint64, i32, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -240,6 +242,13 @@ def get_status(state, stream=None):
 
 def clear_status(state, stream=None):
     _check(load().lq_clear_status(_ptr(state, "state"), _stream(stream)))
+
+
+def debug_set_wait(wait_ns=0, extra_tx_append=0, extra_tx_fold=0):
+    """Test hook: this thread's bound on kernel waits and the bytes the append / fold
+    kernels announce beyond those they copy (so the wait runs out). (0, 0, 0) restores
+    the defaults."""
+    _check(load().lq_debug_set_wait(int(wait_ns), int(extra_tx_append), int(extra_tx_fold)))
 
 
 def state_views(cfg: Config, state, n_states: int) -> dict:

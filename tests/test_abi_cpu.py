@@ -188,3 +188,32 @@ def test_no_gpu_calls_fail_loudly_without_a_device(L):
     rc = L.lq_fold(ctypes.byref(cfg), ctypes.c_void_p(256), 4, None)
     assert rc in (lq.ERR_CUDA, lq.ERR_INVALID_ARG)
     assert lq.last_error() != ""
+
+
+def test_debug_wait_hook_rejects_out_of_range_values(L):
+    with pytest.raises(lq.LQError):
+        lq.debug_set_wait(2_000_000_000, 0, 0)
+    with pytest.raises(lq.LQError):
+        lq.debug_set_wait(0, -1, 0)
+    with pytest.raises(lq.LQError):
+        lq.debug_set_wait(0, 0, 4096)
+    lq.debug_set_wait(1_000_000, 16, 16)
+    lq.debug_set_wait(0, 0, 0)
+
+
+def test_output_overlapping_the_state_buffer_is_refused(L):
+    """o must not overlap the state buffer, which the same kernels read and write; the
+    check runs on the host before anything asks the GPU."""
+    cfg = lq.config()
+    n = 4
+    state = 1 << 32
+    size = lq.state_bytes(cfg, n)
+    far = state + size + (1 << 20)
+    q, k, v, a, b = (far + i * 65536 for i in range(5))
+    for o in (state + 4096, state + size - 16):
+        with pytest.raises(lq.LQError) as e:
+            lq.append(cfg, state, n, q, k, v, a, b, o, stream=0)
+        assert e.value.code == lq.ERR_INVALID_ARG and "state buffer" in str(e.value)
+        with pytest.raises(lq.LQError) as e:
+            lq.decode_step(cfg, state, n, q, k, v, a, b, o, phase=0, stream=0)
+        assert e.value.code == lq.ERR_INVALID_ARG and "state buffer" in str(e.value)
