@@ -38,7 +38,8 @@
  *     another configuration) set the state buffer's status word, which
  *     lq_get_status reads; the affected head-states are left unchanged.
  *   - Threads: no global mutable state except a thread-local error message,
- *     and the thread-local test hook of lq_debug_set_wait.
+ *     the thread-local test hook of lq_debug_set_wait, and the device address
+ *     of lq_decode_step_noalloc's fixed array, looked up once per device.
  *   - n_states = 0 is valid and does nothing.
  */
 #ifndef LQ_H
@@ -218,6 +219,32 @@ int lq_fold(const lq_config* cfg, void* state, int64_t n_states, lq_stream_t str
 int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
                    const float* k, const float* v, const float* alpha, const float* beta, float* o,
                    lq_stream_t stream);
+
+/*
+ * lq_decode_step with phase LQ_PHASE_ANY, for callers that cannot allocate
+ * device memory: an engine that owns all device memory and hands each part of
+ * the model only fixed buffers, where a cudaMalloc on the decode path would
+ * stall the device and can fail once memory is full. The mixed-phase step needs
+ * scratch: a list of the head-states whose window the token fills, and two
+ * counters. lq_decode_step keeps it in the state buffer's work-list plane and
+ * header; this call keeps it instead in a fixed array inside the library's own
+ * device image, 256 KB plus 256 bytes, which every GPU that loads the library
+ * holds until the process exits. It allocates nothing and leaves the state
+ * buffer's work-list plane and header counters untouched. The pages have no
+ * counterpart to this call; it is a deployment variant.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and remembers it; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array. Each call clears the two
+ *     counters first; calls whose kernels may overlap on the GPU (other
+ *     streams, other threads) race on it and must be ordered by the caller.
+ *   - Limits: n_states <= 65536 (LQ_ERR_INVALID_ARG above that); 8-bit codes
+ *     with line compensators (code_bits = 8, comp_fit = 0), else
+ *     LQ_ERR_UNSUPPORTED.
+ * Arguments, results and device-side errors as lq_decode_step.
+ */
+int lq_decode_step_noalloc(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k,
+                           const float* v, const float* alpha, const float* beta, float* o, lq_stream_t stream);
 
 /*
  * One two-record token for every head-state: a token whose update is two

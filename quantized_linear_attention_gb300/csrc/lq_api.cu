@@ -412,6 +412,32 @@ int lq_decode_step(const lq_config* cfg, void* state, int64_t n_states, int32_t 
   return launched(lqi::launch_step(p, (cudaStream_t)stream), "lq_decode_step launch");
 }
 
+int lq_decode_step_noalloc(const lq_config* cfg, void* state, int64_t n_states, const float* q, const float* k,
+                           const float* v, const float* alpha, const float* beta, float* o, lq_stream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (cfg->code_bits != 8 || cfg->comp_fit != 0)
+    return fail(LQ_ERR_UNSUPPORTED, "lq_decode_step_noalloc runs 8-bit codes with line compensators only");
+  if (n_states > lqi::kNoAllocMaxStates)
+    return fail(LQ_ERR_INVALID_ARG, "lq_decode_step_noalloc: n_states %lld exceeds the %d head-states its fixed "
+                "work list holds", (long long)n_states, lqi::kNoAllocMaxStates);
+  int dev = 0;
+  if ((rc = precheck_tokens(cfg, state, n_states, q, k, v, alpha, beta, o)) ||
+      (rc = check_common(cfg, state, n_states, stream, &dev)))
+    return rc;
+  if (n_states == 0) return ok();
+  if ((rc = check_tokens(cfg, n_states, dev, q, k, v, alpha, beta, o, state))) return rc;
+  Params p = make_params(cfg, state, n_states);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.o = o;
+  p.phase = LQ_PHASE_ANY;
+  return launched(lqi::launch_decode_noalloc(p, dev, (cudaStream_t)stream), "lq_decode_step_noalloc launch");
+}
+
 int lq_decode_step2(const lq_config* cfg, void* state, int64_t n_states, int32_t phase, const float* q,
                     const float* k1, const float* v1, const float* beta1, const float* k2, const float* v2,
                     const float* beta2, const float* alpha, float* o, lq_stream_t stream) {

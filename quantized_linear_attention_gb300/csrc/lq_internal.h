@@ -14,6 +14,10 @@ constexpr int kD = 128;       // d_k = d_v
 constexpr int kMaxW = 32;     // records per window
 constexpr int kMaxC = 8;      // compensators per head-state
 constexpr int kThreads = 256; // threads per CTA; one CTA per head-state
+// lq_decode_step_noalloc: head-states its fixed work list holds, and the int32
+// offset of the list in the array (the two counters sit before it).
+constexpr int kNoAllocMaxStates = 65536;
+constexpr int kNoAllocListOffset = 64;
 
 // Device-resident header at offset 0 of every state buffer (256 bytes).
 struct Header {
@@ -62,6 +66,7 @@ struct Params {
   Header* hdr;
   int32_t* counts;
   int32_t* full_list;
+  int32_t* list_ctr;  // lq_decode_step_noalloc: [0] entries on the list, [1] list-fold CTAs done
   uint64_t wait_ns;   // bound on a wait for staged copies (1 s; shorter only under lq_debug_set_wait)
   int32_t dbg_tx_append, dbg_tx_fold;  // test hook: bytes announced beyond those copied (0 normally)
   int8_t* codes;
@@ -110,6 +115,7 @@ cudaError_t launch_step(const Params& p, cudaStream_t st);
 cudaError_t launch_fold(const Params& p, cudaStream_t st);
 cudaError_t launch_init_range(const Params& p, int64_t count, cudaStream_t st);
 cudaError_t launch_fold_listed(const Params& p, cudaStream_t st);
+cudaError_t launch_decode_noalloc(const Params& p, int dev, cudaStream_t st);
 cudaError_t launch_export(const Params& p, cudaStream_t st);
 cudaError_t launch_fp32_step(const Fp32Params& p, cudaStream_t st);
 

@@ -39,6 +39,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "lq_internal.h"
 
 namespace lqi {
@@ -2369,7 +2371,9 @@ __device__ __forceinline__ void prefetch_key(const Params& p, int64_t s, int n0,
 // into registers before the staging wait -- at once when the phase is stated,
 // else once thread 0 has read the record count. With p.push_full the
 // head-states whose window this token fills are put on the full-window list.
-template <bool KDA, int BITS, bool FIT>
+// SLIST: the work list and its counters live in the library's fixed device
+// array (lq_decode_step_noalloc) instead of the state buffer.
+template <bool KDA, int BITS, bool FIT, bool SLIST = false>
 __global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -2397,7 +2401,7 @@ __global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
   if (threadIdx.x == 0) {
     p.counts[s] = n0 + 1;
     if (p.push_full && n0 + 1 == p.W) {
-      const int slot = atomicAdd(&p.hdr->full_n, 1);
+      const int slot = atomicAdd(SLIST ? &p.list_ctr[0] : &p.hdr->full_n, 1);
       if (slot >= 0 && slot < p.n_states)
         p.full_list[slot] = (int32_t)s;
       else
@@ -2565,7 +2569,7 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
 // b + 2G, ... (G = gridDim.x, at most the CTAs that fit on the GPU at once),
 // so the few head-states whose window fills this token are spread over every
 // SM. Each entry must hold W records. The last CTA to finish empties the list.
-template <bool KDA, int BITS, bool FIT>
+template <bool KDA, int BITS, bool FIT, bool SLIST = false>
 __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
@@ -2573,7 +2577,7 @@ __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
   if (threadIdx.x == 0) {
     int nf = -1;
     if (header_ok(p)) {
-      nf = *reinterpret_cast<volatile int32_t*>(&p.hdr->full_n);
+      nf = *reinterpret_cast<volatile int32_t*>(SLIST ? &p.list_ctr[0] : &p.hdr->full_n);
       if (nf < 0 || nf > p.n_states) {
         if (blockIdx.x == 0) set_error(p, LQ_ERR_STATE, -1);
         nf = 0;
@@ -2603,7 +2607,12 @@ __global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
   }
   if (threadIdx.x == 0) {
     __threadfence();
-    if (atomicAdd(&p.hdr->fold_done, 1) == (int)gridDim.x - 1) {
+    if (SLIST) {
+      if (atomicAdd(&p.list_ctr[1], 1) == (int)gridDim.x - 1) {
+        p.list_ctr[0] = 0;
+        p.list_ctr[1] = 0;
+      }
+    } else if (atomicAdd(&p.hdr->fold_done, 1) == (int)gridDim.x - 1) {
       p.hdr->full_n = 0;
       p.hdr->fold_done = 0;
     }
@@ -2774,10 +2783,9 @@ cudaError_t launch_fold(const Params& p, cudaStream_t st) {
 }
 
 // As many CTAs as fit on the GPU at once (never more than head-states).
-cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, p.W, p.W, false, true, true);
+template <typename K>
+static cudaError_t launch_listed(K kernel, const Params& q, cudaStream_t st) {
   const int smem = smem_of(q, true);
-  auto kernel = LQ_PICK2(k_fold_listed, q);
   cudaError_t e = set_smem(kernel, smem);
   int dev = 0, sms = 0, per_sm = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
@@ -2785,9 +2793,63 @@ cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, (size_t)smem);
   if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
-  if (grid > p.n_states) grid = p.n_states;
+  if (grid > q.n_states) grid = q.n_states;
   kernel<<<dim3((unsigned)grid), dim3(256), (size_t)smem, st>>>(q);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
+  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  return launch_listed(LQ_PICK2(k_fold_listed, q), q, st);
+}
+
+// ---------------------------------------------------------------------------
+// lq_decode_step_noalloc: the mixed-phase step with its work list in a fixed
+// array of this library's own device image. Every call on a device shares it
+// and it keeps what the last call left there; the two counters (entries on the
+// list, list-fold CTAs done) are cleared at the start of every call, and the
+// entries are written before they are read. Calls whose kernels overlap on the
+// GPU race on it.
+static __device__ __align__(256) int32_t lq_noalloc_scratch[kNoAllocListOffset + kNoAllocMaxStates];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of lq_noalloc_scratch on device `dev` (the current device),
+// looked up once per device with that device current. In host code the
+// array's name stands for a host-side shadow, not a device address, so it is
+// never passed to a kernel directly.
+static cudaError_t noalloc_scratch(int dev, int32_t** out) {
+  static std::mutex mu;
+  static int32_t* addr[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, lq_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_noalloc(const Params& p, int dev, cudaStream_t st) {
+  int32_t* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(dev, &scratch);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(scratch, 0, 2 * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  Params r = p;
+  r.push_full = 1;
+  r.list_ctr = scratch;
+  r.full_list = scratch + kNoAllocListOffset;
+  const Params a = with_layout(r, append_slots(r.W, r.phase), 0, true, false, false, false, false, !r.kda);
+  e = a.kda ? launch(k_append<true, 8, false, true>, a, smem_of(a, false), st, 128)
+            : launch(k_append<false, 8, false, true>, a, smem_of(a, false), st, 128);
+  if (e != cudaSuccess) return e;
+  const Params f = with_layout(r, r.W, r.W, false, true, true);
+  return f.kda ? launch_listed(k_fold_listed<true, 8, false, true>, f, st)
+               : launch_listed(k_fold_listed<false, 8, false, true>, f, st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "LQ_OK", -1: "LQ_ERR_INVALID_ARG", -2: "LQ_ERR_UNSUPPORTED", 
 
 # Every symbol include/lq.h declares.
 EXPORTS = ("lq_config_default", "lq_state_bytes", "lq_layout", "lq_state_init", "lq_state_init_range", "lq_append",
-           "lq_fold", "lq_decode_step", "lq_decode_step2", "lq_decode_step_rwkv7", "lq_export_state",
+           "lq_fold", "lq_decode_step", "lq_decode_step_noalloc", "lq_decode_step2", "lq_decode_step_rwkv7", "lq_export_state",
            "lq_fp32_decode_step", "lq_get_status", "lq_clear_status", "lq_last_error", "lq_version",
            "lq_debug_set_wait")
 
@@ -83,6 +83,7 @@ def load():
         "lq_append": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_fold": (ctypes.c_int, [cfgp, P, i64, P]),
         "lq_decode_step": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P]),
+        "lq_decode_step_noalloc": (ctypes.c_int, [cfgp, P, i64, P, P, P, P, P, P, P]),
         "lq_decode_step2": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P, P, P, P]),
         "lq_decode_step_rwkv7": (ctypes.c_int, [cfgp, P, i64, i32, P, P, P, P, P, P, P, P]),
         "lq_export_state": (ctypes.c_int, [cfgp, P, i64, P, P]),
@@ -199,6 +200,15 @@ def decode_step(cfg, state, n_states, q, k, v, alpha, beta, o, phase=PHASE_ANY, 
     _check(load().lq_decode_step(ctypes.byref(cfg), _ptr(state, "state"), n_states, int(phase), _ptr(q, "q", f),
                                  _ptr(k, "k", f), _ptr(v, "v", f), _ptr(alpha, "alpha", f), _ptr(beta, "beta", f),
                                  _ptr(o, "o", f), _stream(stream)))
+
+
+def decode_step_noalloc(cfg, state, n_states, q, k, v, alpha, beta, o, stream=None):
+    """Mixed-phase decode step whose work list lives in the library's fixed device array
+    (for callers that cannot allocate device memory); arguments as ``decode_step``."""
+    f = _f32()
+    _check(load().lq_decode_step_noalloc(ctypes.byref(cfg), _ptr(state, "state"), n_states, _ptr(q, "q", f),
+                                         _ptr(k, "k", f), _ptr(v, "v", f), _ptr(alpha, "alpha", f),
+                                         _ptr(beta, "beta", f), _ptr(o, "o", f), _stream(stream)))
 
 
 def decode_step2(cfg, state, n_states, q, k1, v1, beta1, k2, v2, beta2, alpha, o, phase=PHASE_ANY, stream=None):
