@@ -45,7 +45,19 @@ UNIT = "head-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_append_gdn_batch128.md")
 PROFILE_STEP = os.path.join(ROOT, "profiles", "k_step_gdn_batch128.md")
-KERNEL_SOURCE = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc", "lq_kernels.cu")
+CSRC = os.path.join(ROOT, "quantized_linear_attention_gb300", "csrc")
+
+
+def kernel_sources_sha256():
+    """One hash over every CUDA source and header of the library (sorted by name), so a
+    profile summary taken on other kernels is recognised as stale."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
 
 
 # ----------------------------------------------------------------------------- bytes
@@ -137,8 +149,7 @@ def profile_traffic(n_states, summary=PROFILE_SUMMARY):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
-    if fields.get("kernel_source_sha256") != src:
+    if fields.get("kernel_sources_sha256") != kernel_sources_sha256():
         return None, "kernel changed since the ncu capture"
     try:
         per = float(fields["dram_bytes_per_launch"])

@@ -47,6 +47,8 @@ struct Stage {
   int k2n_b, zk2_b, basek2, g2, ec2;
   // RWKV7 tokens: the erase key and the decay products of the held records
   int en_b, Pp_b;
+  // append-only step: the smoothed read vectors as duplicated pairs
+  int zdk, zdq;
   int end;
 };
 
@@ -109,6 +111,7 @@ struct Fp32Params {
 
 cudaError_t launch_init(const Params& p, cudaStream_t st);
 cudaError_t launch_append(const Params& p, cudaStream_t st);
+cudaError_t launch_append_slist(const Params& p, cudaStream_t st);
 cudaError_t launch_append2(const Params& p, cudaStream_t st);
 cudaError_t launch_append_rwkv(const Params& p, cudaStream_t st);
 cudaError_t launch_step(const Params& p, cudaStream_t st);
