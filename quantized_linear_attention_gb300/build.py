@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 
-CUDA_SOURCES = ["lq_kernels.cu", "lq_append.cu", "lq_fp32.cu", "lq_api.cu"]
+CUDA_SOURCES = ["lq_kernels.cu", "lq_append.cu", "lq_step.cu", "lq_fp32.cu", "lq_api.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

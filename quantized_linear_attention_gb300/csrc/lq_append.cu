@@ -37,51 +37,9 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "lq_device.cuh"
+#include "lq_append.cuh"
 
 namespace lqi {
-
-// Interleaved blocked layout of the matvec's read pairs: lane qq's block
-// (columns 16qq..16qq+15) holds (lambda . y_j, lambda . A . q_j) for each of
-// its columns, 32 floats from float 36 qq; the 4 floats of padding per block
-// put the 8 lanes of a lane group on distinct banks for 16-byte loads.
-constexpr int kDS = 36;
-constexpr int kDupLen = 8 * kDS;
-__device__ __forceinline__ int dv2(int j) { return kDS * (j >> 4) + 2 * (j & 15); }
-
-__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 f2_shfl_xor(f32x2 v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
-
-// The four codes e0..e0+3 (e0 a multiple of 4) of one lane's 16-code block of a
-// row, as code_words gives its words, converted exactly in two packed pairs of
-// codes from one word each: two byte permutes put c + bias in the mantissas of
-// 2^23 and one packed subtraction removes the bias. 8-bit codes: p = (e0, e0+1),
-// q = (e0+2, e0+3). 4- and 6-bit codes (even and odd codes in different
-// words): p = (e0, e0+2), q = (e0+1, e0+3).
-template <int BITS>
-__device__ __forceinline__ void code_quad(const uint32_t (&cw)[4], int e0, f32x2& p, f32x2& q) {
-  constexpr float bias = BITS == 8 ? 8388736.0f : (BITS == 6 ? 8388640.0f : 8388616.0f);
-  const f32x2 b2 = f2_pack(bias, bias);
-  if (BITS == 8) {
-    const uint32_t w = cw[e0 >> 2];
-    p = f2_sub(f2_bits(__byte_perm(w, 0x4B000000u, 0x7540u), __byte_perm(w, 0x4B000000u, 0x7541u)), b2);
-    q = f2_sub(f2_bits(__byte_perm(w, 0x4B000000u, 0x7542u), __byte_perm(w, 0x4B000000u, 0x7543u)), b2);
-  } else {
-    const uint32_t we = cw[2 * (e0 >> 3)], wo = cw[2 * (e0 >> 3) + 1];
-    const uint32_t b = (uint32_t)((e0 & 7) >> 1);  // byte of e0 (and e0+1); e0+2 sits at b + 1
-    p = f2_sub(f2_bits(__byte_perm(we, 0x4B000000u, 0x7540u | b), __byte_perm(we, 0x4B000000u, 0x7540u | (b + 1))),
-               b2);
-    q = f2_sub(f2_bits(__byte_perm(wo, 0x4B000000u, 0x7540u | b), __byte_perm(wo, 0x4B000000u, 0x7540u | (b + 1))),
-               b2);
-  }
-}
-
-// f in both halves of a pair: the packed fma takes it as a broadcast operand.
-__device__ __forceinline__ f32x2 f2_dup(float f) { return f2_pack(f, f); }
 
 // Thread 0: barrier init, the record count (read first only when the phase is
 // not stated) and the bulk copies of what the matvec and the row pass read --
@@ -154,28 +112,6 @@ __device__ __forceinline__ StageInfo append_start(const Params& p, int64_t s, in
   return *sh;
 }
 
-// The new record's output term k . q (P_n = 1), in one warp: lane l holds
-// elements 4l..4l+3, and the sum is compensated (each product split into its
-// float value and its exact error by an fma, the values added by error-free
-// two-sums with the errors carried beside them), as if summed in twice the
-// working precision and rounded once.
-__device__ __forceinline__ float kq_dot2_warp(const float4 a, const float4 b) {
-  float s = __fmul_rn(a.x, b.x), c = __fmaf_rn(a.x, b.x, -s);
-  const float xs[3] = {a.y, a.z, a.w}, ys[3] = {b.y, b.z, b.w};
-#pragma unroll
-  for (int t = 0; t < 3; ++t) {
-    const float pr = __fmul_rn(xs[t], ys[t]);
-    two_sum_into(s, c, pr, __fmaf_rn(xs[t], ys[t], -pr));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float o = __shfl_xor_sync(0xffffffffu, s, off);
-    const float oc = __shfl_xor_sync(0xffffffffu, c, off);
-    two_sum_into(s, c, o, oc);
-  }
-  return __fadd_rn(s, c);
-}
-
 // One token appended to every head-state (no fold): the W-1 decode steps that
 // cannot fill the window, lq_append, and the first kernel of a mixed-phase
 // step (p.push_full: the head-states whose window this token fills go on the
@@ -196,17 +132,9 @@ __global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
   const int64_t s = blockIdx.x;
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid >> 3) & 3, qq = tid & 7, grp = tid >> 3;
-  const Stage& L = p.st;
-  char* sm = lq_dyn_smem;
-  float* P = at<float>(sm, L.P);
-  float* P_b = at<float>(sm, L.P_b);
-  float* kn_b = at<float>(sm, L.kn_b);
-  float* qn_b = at<float>(sm, L.qn_b);
-  float* zkq = at<float>(sm, L.zdk);  // (lambda . y_j, lambda . A . q_j), interleaved blocks
-  float* g = at<float>(sm, L.g);
-  float* h = at<float>(sm, L.h);
-  float* ec = at<float>(sm, L.ec);
-  float* eq = at<float>(sm, L.eq);
+  const AppendSmem a = append_smem(p.st, lq_dyn_smem);
+  float* P = a.P();
+  float* P_b = a.P_b();
   const int known = (p.phase >= 0 && p.phase < W) ? p.phase : -1;
 
   // Lane bits (b0, b1, b2) of qq and the row this lane finishes: m = 4 b0 + 2 b1 + b2.
@@ -272,73 +200,11 @@ __global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
     } else {
       A = P[0];
     }
-    const int jb = bv(tid);
-    kn_b[jb] = kj;
-    qn_b[jb] = qj;
-    *reinterpret_cast<float2*>(zkq + dv2(tid)) =
-        make_float2(__fmul_rn(lamj, __fmul_rn(A, kj)), __fmul_rn(lamj, __fmul_rn(A, qj)));
+    append_vectors(a, tid, kj, qj, lamj, A);
   }
   __syncthreads();
 
-  // A4 record dots, one lane group each (record m = g + 1, then g + 17), while
-  // the copies land: g_m = k_m . (P_m . k_n) in the canonical order, and the
-  // output side h_m = k_m . (P_m . q_n) (order free: two interleaved chains).
-  for (int base = 0; base < n0; base += 16) {
-    const int job = base + grp;
-    float pa = 0.0f;
-    f32x2 pq = f2_pack(0.0f, 0.0f);
-    if (job < n0) {
-      const int m = job + 1;
-      float4 kv[4];
-      if (base == 0) {
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) kv[c4] = kpre[c4];
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(p.rec_k + (s * W + job) * kD + 16 * qq);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) kv[c4] = src[c4];
-      }
-      const ulonglong2* kx2 = reinterpret_cast<const ulonglong2*>(kn_b + 20 * qq);
-      const ulonglong2* qx2 = reinterpret_cast<const ulonglong2*>(qn_b + 20 * qq);
-      const ulonglong2* pm2 = reinterpret_cast<const ulonglong2*>(P_b + m * kBV + 20 * qq);
-      const float pms = KDA ? 0.0f : P[m];
-      const f32x2 pmp = f2_pack(pms, pms);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const ulonglong2 kx = kx2[c4], qx = qx2[c4];
-        f32x2 pa01 = pmp, pa23 = pmp;
-        if (KDA) {
-          const ulonglong2 pmv = pm2[c4];
-          pa01 = pmv.x;
-          pa23 = pmv.y;
-        }
-        float x0, x1, x2, x3;
-        f2_unpack(f2_mul(pa01, kx.x), x0, x1);
-        f2_unpack(f2_mul(pa23, kx.y), x2, x3);
-        const float4 kvc = kv[c4];
-        pa = __fmaf_rn(kvc.x, x0, pa);
-        pa = __fmaf_rn(kvc.y, x1, pa);
-        pa = __fmaf_rn(kvc.z, x2, pa);
-        pa = __fmaf_rn(kvc.w, x3, pa);
-        const f32x2 k01 = f2_pack(kvc.x, kvc.y), k23 = f2_pack(kvc.z, kvc.w);
-        if (KDA) {
-          pq = f2_fma(k01, f2_mul(pa01, qx.x), pq);
-          pq = f2_fma(k23, f2_mul(pa23, qx.y), pq);
-        } else {
-          pq = f2_fma(k01, qx.x, pq);  // GDN: scaled by P_m after the tree
-          pq = f2_fma(k23, qx.y, pq);
-        }
-      }
-    }
-    float q0, q1;
-    f2_unpack(pq, q0, q1);
-    pa = tree8(pa);
-    const float pb = tree8(__fadd_rn(q0, q1));
-    if (job < n0 && qq == 0) {
-      g[job] = pa;
-      h[job] = KDA ? pb : __fmul_rn(P[job + 1], pb);
-    }
-  }
+  record_dots<KDA, true>(p, s, W, n0, a, kpre, nullptr);
 
   if (w == 3) {  // the new record's output term, while the copies land
     const float d = kq_dot2_warp(k4, q4);
@@ -352,158 +218,10 @@ __global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
     p.rec_alpha[s * p.alpha_stride + (n - 1) * kD + tid] = aj;
   else if (tid == 0)
     p.rec_alpha[s * p.alpha_stride + (n - 1)] = alpha_s;
-  const int32_t* cid = at<int32_t>(sm, L.comp_id);
-  const float* cl = at<float>(sm, L.comp_line);
-
-  // A3: lane group c forms compensator c's two sums, ec_c = b_c . y with
-  // y = A . k_n (canonical order) and eq_c = b_c . (A . q_n) (order free). A row
-  // compensator (and every fitted factor) takes a full dot. A column
-  // compensator's dot with y is y[j0] itself: the other terms of its chain are
-  // fmas with zero coefficients, which leave +0 and a nonzero partial
-  // unchanged, so the canonical dot is y[j0] + 0.
-  if (w * 4 < C) {
-    const int c = grp < C ? grp : C - 1;
-    const int id = cid[c];
-    const bool dense = FIT || id < kD;
-    float pa = 0.0f;
-    f32x2 pq = f2_pack(0.0f, 0.0f);
-    if (dense) {
-      const float4* b4 = reinterpret_cast<const float4*>(cl + (FIT ? (2 * c + 1) * kD : c * kD) + 16 * qq);
-      const ulonglong2* kx2 = reinterpret_cast<const ulonglong2*>(kn_b + 20 * qq);
-      const ulonglong2* qx2 = reinterpret_cast<const ulonglong2*>(qn_b + 20 * qq);
-      const ulonglong2* a02 = reinterpret_cast<const ulonglong2*>(P_b + 20 * qq);
-      const f32x2 a0p = f2_pack(KDA ? 0.0f : P[0], KDA ? 0.0f : P[0]);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const float4 bb = b4[c4];
-        const ulonglong2 kx = kx2[c4], qx = qx2[c4];
-        f32x2 a01 = a0p, a23 = a0p;
-        if (KDA) {
-          const ulonglong2 av = a02[c4];
-          a01 = av.x;
-          a23 = av.y;
-        }
-        float y0, y1, y2, y3;
-        f2_unpack(f2_mul(a01, kx.x), y0, y1);
-        f2_unpack(f2_mul(a23, kx.y), y2, y3);
-        pa = __fmaf_rn(bb.x, y0, pa);
-        pa = __fmaf_rn(bb.y, y1, pa);
-        pa = __fmaf_rn(bb.z, y2, pa);
-        pa = __fmaf_rn(bb.w, y3, pa);
-        pq = f2_fma(f2_pack(bb.x, bb.y), f2_mul(a01, qx.x), pq);
-        pq = f2_fma(f2_pack(bb.z, bb.w), f2_mul(a23, qx.y), pq);
-      }
-    }
-    float q0, q1;
-    f2_unpack(pq, q0, q1);
-    pa = tree8(pa);
-    const float pb = tree8(__fadd_rn(q0, q1));
-    if (grp < C && qq == 0) {
-      if (dense) {
-        ec[c] = pa;
-        eq[c] = pb;
-      } else {
-        const int jb = bv(id - kD);
-        const float A0 = KDA ? P_b[jb] : P[0];
-        ec[c] = __fadd_rn(__fmul_rn(A0, kn_b[jb]), 0.0f);
-        eq[c] = __fmul_rn(A0, qn_b[jb]);
-      }
-    }
-  }
+  comp_dots<KDA, FIT>(C, a);
   __syncthreads();  // the dots are visible to every row pass
 
-  // A2: the fused dequantize + two matvecs. Slot t of the lane holds the pair
-  // (k chain, q chain) of row row0 + (t ^ m); in the exchange steps the lane
-  // keeps slots 0..3, 0..1, 0 and sends the rest, so it ends with row irow.
-  float basek, baseq;
-  {
-    const float* zp = zkq + kDS * qq;
-    const int8_t* cb = at<int8_t>(sm, L.codes);
-    uint32_t cw[8][4];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) code_words<BITS>(cb + (row0 + (t ^ mrow)) * row_bytes<BITS>(), qq, cw[t]);
-    f32x2 acc[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = f2_pack(0.0f, 0.0f);
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {  // columns 16qq + 4c4 .. +3, in ascending order
-      const ulonglong2 z01 = *reinterpret_cast<const ulonglong2*>(zp + 8 * c4);
-      const ulonglong2 z23 = *reinterpret_cast<const ulonglong2*>(zp + 8 * c4 + 4);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        f32x2 fp, fq;
-        code_quad<BITS>(cw[t], 4 * c4, fp, fq);
-        float f0, f1, f2, f3;  // codes 4c4 + 0..3
-        if (BITS == 8) {
-          f2_unpack(fp, f0, f1);
-          f2_unpack(fq, f2, f3);
-        } else {
-          f2_unpack(fp, f0, f2);
-          f2_unpack(fq, f1, f3);
-        }
-        acc[t] = f2_fma(f2_dup(f0), z01.x, acc[t]);
-        acc[t] = f2_fma(f2_dup(f1), z01.y, acc[t]);
-        acc[t] = f2_fma(f2_dup(f2), z23.x, acc[t]);
-        acc[t] = f2_fma(f2_dup(f3), z23.y, acc[t]);
-      }
-    }
-    // the canonical tree ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)) over the lane group
-#pragma unroll
-    for (int t = 0; t < 4; ++t) acc[t] = f2_add(acc[t], f2_shfl_xor(acc[t + 4], 1));
-#pragma unroll
-    for (int t = 0; t < 2; ++t) acc[t] = f2_add(acc[t], f2_shfl_xor(acc[t + 2], 2));
-    acc[0] = f2_add(acc[0], f2_shfl_xor(acc[1], 4));
-    float tk, tq;
-    f2_unpack(acc[0], tk, tq);
-    const float sg = at<float>(sm, L.sigma)[irow];
-    basek = __fmul_rn(sg, tk);
-    baseq = __fmul_rn(sg, tq);
-  }
-
-  // A3-A5 for value row i = irow, in this lane: acc = base; the compensators in
-  // order, each as its expanded rank-one term (a_c[i] is a column
-  // compensator's line entry, or 1 / 0 on / off a row compensator's own row);
-  // the records in order; u_n = beta (v - acc). A6: the output in any order.
-  {
-    const int i = irow;
-    float acc = basek;
-    float oo = baseq;
-#pragma unroll
-    for (int c = 0; c < CMAX; ++c) {
-      if (c < C) {
-        float a;
-        if (FIT) {
-          a = cl[2 * c * kD + i];
-        } else {
-          const int id = cid[c];
-          a = id >= kD ? cl[c * kD + i] : (id == i ? 1.0f : 0.0f);
-        }
-        acc = __fmaf_rn(a, ec[c], acc);
-        oo = __fmaf_rn(a, eq[c], oo);
-      }
-    }
-    const float* rui = at<float>(sm, L.rec_u) + i;
-#pragma unroll
-    for (int m0 = 0; m0 < WMAX - 1; m0 += 4) {
-      if (m0 < n - 1) {
-        const float4 g4 = *reinterpret_cast<const float4*>(g + m0);
-        const float4 h4 = *reinterpret_cast<const float4*>(h + m0);
-        const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, hs[4] = {h4.x, h4.y, h4.z, h4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (m0 + e < n - 1) {
-            const float um = rui[(m0 + e) * kD];
-            acc = __fmaf_rn(um, gs[e], acc);
-            oo = __fmaf_rn(um, hs[e], oo);
-          }
-        }
-      }
-    }
-    const float u = __fmul_rn(beta, __fsub_rn(vi, acc));
-    oo = __fmaf_rn(u, s_kq, oo);
-    p.rec_u[rec_off + i] = u;
-    p.o[s * kD + i] = oo;
-  }
+  (void)matvec_row_pass<KDA, BITS, FIT, CMAX, WMAX>(p, s, C, n, rec_off, vi, beta, s_kq, a);
   if (tid == 0) {
     p.counts[s] = n;
     if (p.push_full && n == W) {

@@ -136,6 +136,40 @@ __host__ __device__ constexpr int row_bytes() {
   return kD * BITS / 8;
 }
 
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_shfl_xor(f32x2 v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+
+// The four codes e0..e0+3 (e0 a multiple of 4) of one lane's 16-code block of a
+// row, as code_words gives its words, converted exactly in two packed pairs of
+// codes from one word each: two byte permutes put c + bias in the mantissas of
+// 2^23 and one packed subtraction removes the bias. 8-bit codes: p = (e0, e0+1),
+// q = (e0+2, e0+3). 4- and 6-bit codes (even and odd codes in different
+// words): p = (e0, e0+2), q = (e0+1, e0+3).
+template <int BITS>
+__device__ __forceinline__ void code_quad(const uint32_t (&cw)[4], int e0, f32x2& p, f32x2& q) {
+  constexpr float bias = BITS == 8 ? 8388736.0f : (BITS == 6 ? 8388640.0f : 8388616.0f);
+  const f32x2 b2 = f2_pack(bias, bias);
+  if (BITS == 8) {
+    const uint32_t w = cw[e0 >> 2];
+    p = f2_sub(f2_bits(__byte_perm(w, 0x4B000000u, 0x7540u), __byte_perm(w, 0x4B000000u, 0x7541u)), b2);
+    q = f2_sub(f2_bits(__byte_perm(w, 0x4B000000u, 0x7542u), __byte_perm(w, 0x4B000000u, 0x7543u)), b2);
+  } else {
+    const uint32_t we = cw[2 * (e0 >> 3)], wo = cw[2 * (e0 >> 3) + 1];
+    const uint32_t b = (uint32_t)((e0 & 7) >> 1);  // byte of e0 (and e0+1); e0+2 sits at b + 1
+    p = f2_sub(f2_bits(__byte_perm(we, 0x4B000000u, 0x7540u | b), __byte_perm(we, 0x4B000000u, 0x7540u | (b + 1))),
+               b2);
+    q = f2_sub(f2_bits(__byte_perm(wo, 0x4B000000u, 0x7540u | b), __byte_perm(wo, 0x4B000000u, 0x7540u | (b + 1))),
+               b2);
+  }
+}
+
+// f in both halves of a pair: the packed fma takes it as a broadcast operand.
+__device__ __forceinline__ f32x2 f2_dup(float f) { return f2_pack(f, f); }
+
 // Sum of the 8 block partials of a lane group in the fixed tree order.
 __device__ __forceinline__ float tree8(float x) {
   x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, 1));
@@ -322,6 +356,14 @@ __host__ __device__ __forceinline__ int bv(int j) { return j + ((j >> 4) << 2); 
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
+// Interleaved blocked layout of the append matvec's read pairs: lane qq's block
+// (columns 16qq..16qq+15) holds (lambda . y_j, lambda . A . q_j) for each of
+// its columns, 32 floats from float 36 qq; the 4 floats of padding per block
+// put the 8 lanes of a lane group on distinct banks for 16-byte loads.
+constexpr int kDS = 36;
+constexpr int kDupLen = 8 * kDS;
+__host__ __device__ inline int dv2(int j) { return kDS * (j >> 4) + 2 * (j & 15); }
+
 // slots_u: staged record slots of u and alpha; slots_k: staged slots of k (0
 // when the keys travel in registers). The token's q, k, v (and alpha) are read
 // into registers, not staged.
@@ -346,14 +388,16 @@ __host__ __device__ inline Stage stage_layout(int W, int C, int kda, int comp_id
   L.rec_alpha = take(!stage_alpha ? 0 : kda ? 4 * kD * slots_u : 4 * ((W + 3) / 4 * 4));
   L.kn_b = take(va * 4 * kBV);
   L.qn_b = take(va * 4 * kBV);
-  L.zk_b = take(va * 4 * kBV);
-  L.zq_b = take(va * 4 * kBV);
+  const int vo = (append && !fold) ? 1 : 0;  // arrays of the two-record and RWKV7 appends only
+  L.zk_b = take(vo * 4 * kBV);
+  L.zq_b = take(vo * 4 * kBV);
+  L.zdk = take(va * fo * 4 * kDupLen);  // the fused step's append reads its matvec pairs here
   L.lam_b = take(fo * 4 * kBV);
   L.kd_b = take(fo * 4 * kBV * W);
   L.bd_b = take(fo * 4 * kBV * C);
   L.P_b = take(kda * 4 * kBV * (W + 1));
-  L.basek = take(va * 4 * kD);
-  L.baseq = take(va * 4 * kD);
+  L.basek = take(vo * 4 * kD);
+  L.baseq = take(vo * 4 * kD);
   L.P = take(4 * (W + 1));
   L.g = take(4 * (W + 1));
   L.h = take(4 * (W + 1));
