@@ -8,6 +8,7 @@
 // step; fastpathlabs.ai research note 4, "What we built".
 #pragma once
 
+
 #include "lq_device.cuh"
 
 namespace lqi {
@@ -130,7 +131,9 @@ __device__ __forceinline__ void fold_tables(const Params& p, int n, const Stage&
 // F1 for the 4 rows x 16 columns a thread owns: S_ij = ((sigma_i Cd_ij)
 // lambda_j) P_0[j], then the compensators in order, then the records in order,
 // each an fma. Adjacent columns (2k, 2k+1) of a row travel as one packed pair.
-template <bool KDA, int BITS, bool FIT>
+// NREC: the record count when fixed at compile time (the fused step of the
+// pages' configuration folds W = 16 records), 0 when given by n.
+template <bool KDA, int BITS, bool FIT, int NREC = 0>
 __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const Stage& L, char* sm, float acc[4][16]) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
@@ -252,28 +255,30 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
       }
     }
   }
-  // Records in order. Each record's key block is read once, in two halves of
-  // eight columns (four pairs), and its correction u_m[i] of each row is
-  // broadcast into both halves of the packed fma.
-#pragma unroll 1
-  for (int m = 0; m < n; ++m) {
+  // Records in order. Each record's key block is read once, four columns (two
+  // pairs) at a time, and its correction u_m[i] of each row is broadcast into
+  // both halves of the packed fma.
+  const float* Ui = U + 4 * w + r;
+  auto record = [&](int m) {
     const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(kd_b + m * kBV + 20 * qq);
     float u[4];
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) u[pp] = U[m * kD + 32 * pp + 4 * w + r];
+    for (int pp = 0; pp < 4; ++pp) u[pp] = Ui[m * kD + 32 * pp];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const ulonglong2 ka = k4[2 * hf], kb = k4[2 * hf + 1];
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const ulonglong2 kq = k4[c4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
         const f32x2 u2 = f2_pack(u[pp], u[pp]);
-        a2[pp][4 * hf] = f2_fma(u2, ka.x, a2[pp][4 * hf]);
-        a2[pp][4 * hf + 1] = f2_fma(u2, ka.y, a2[pp][4 * hf + 1]);
-        a2[pp][4 * hf + 2] = f2_fma(u2, kb.x, a2[pp][4 * hf + 2]);
-        a2[pp][4 * hf + 3] = f2_fma(u2, kb.y, a2[pp][4 * hf + 3]);
+        a2[pp][2 * c4] = f2_fma(u2, kq.x, a2[pp][2 * c4]);
+        a2[pp][2 * c4 + 1] = f2_fma(u2, kq.y, a2[pp][2 * c4 + 1]);
       }
     }
-  }
+  };
+  // one record per iteration: unrolling adds instructions (measured: 24,760
+  // warp instructions per head-state in the fused step against 28,770 at four)
+#pragma unroll 1
+  for (int m = 0; m < (NREC ? NREC : n); ++m) record(m);
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp)
 #pragma unroll
@@ -349,23 +354,28 @@ __device__ __forceinline__ void column_quads(const float* S, float* colpart) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) off[k] = (cq ^ ((((cq >> 3) + k) & 3) | (k & 4))) << 2;
   const float* base = S + 16 * b * kD;
-  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+  if (SQUARES) {
+    // each column's chain in its own half of a packed pair
+    f32x2 s01 = f2_pack(0.0f, 0.0f), s23 = s01;
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const float4 x = *reinterpret_cast<const float4*>(base + t * kD + off[t & 7]);
-    if (SQUARES) {
-      a0 = __fmaf_rn(x.x, x.x, a0);
-      a1 = __fmaf_rn(x.y, x.y, a1);
-      a2 = __fmaf_rn(x.z, x.z, a2);
-      a3 = __fmaf_rn(x.w, x.w, a3);
-    } else {
+    for (int t = 0; t < 16; ++t) {
+      const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(base + t * kD + off[t & 7]);
+      s01 = f2_fma(x.x, x.x, s01);
+      s23 = f2_fma(x.y, x.y, s23);
+    }
+    *reinterpret_cast<ulonglong2*>(colpart + b * kD + 4 * cq) = make_ulonglong2(s01, s23);
+  } else {
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const float4 x = *reinterpret_cast<const float4*>(base + t * kD + off[t & 7]);
       a0 = __fadd_rn(a0, fabsf(x.x));
       a1 = __fadd_rn(a1, fabsf(x.y));
       a2 = __fadd_rn(a2, fabsf(x.z));
       a3 = __fadd_rn(a3, fabsf(x.w));
     }
+    *reinterpret_cast<float4*>(colpart + b * kD + 4 * cq) = make_float4(a0, a1, a2, a3);
   }
-  *reinterpret_cast<float4*>(colpart + b * kD + 4 * cq) = make_float4(a0, a1, a2, a3);
 }
 
 // F2, fitted-factor reading of the compensators (LeapQuant §3.3: dominant
@@ -798,10 +808,12 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     }
     __syncthreads();
     const int win = s_win;
+    const bool last = c == p.C - 1;  // no later round reads the refreshed scores
     float* line = p.comp_line + (s * p.C + c) * kD;
     if (win < kD) {
       const int b = win >> 4;
       if (tid < kD) {
+        if (!last) {
         // column j = tid: block-b chain over rows 16b..16b+15 without row win
         const float* base = S + 16 * b * kD;
         float acc = 0.0f;
@@ -812,6 +824,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         }
         tl.colpart[b * kD + tid] = acc;
         nxt[kD + tid] = tree8_mem(tl.colpart + tid, kD);
+        }
       } else {
         const int t2 = tid - kD;  // row t2's score carries over
         nxt[t2] = t2 == win ? 0.0f : cur[t2];
@@ -828,6 +841,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
     } else {
       const int js = win - kD, q = js >> 4;
       if (tid < kD) {
+        if (!last) {
         // row i = tid: block-q chain over columns 16q..16q+15 without column js
         const int i = tid;
         int ro[4];
@@ -843,6 +857,7 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
         }
         tl.rowpart[i * 8 + q] = acc;
         nxt[i] = tree8_mem(tl.rowpart + i * 8, 1);
+        }
       } else {
         const int i = tid - kD;  // column i's score carries over
         nxt[kD + i] = kD + i == win ? 0.0f : cur[kD + i];

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256, 3) k_step(Params p) {
   __syncthreads();
 
   float acc[4][16];
-  reconstruct_rows<KDA, BITS, FIT>(p, n, L, sm, acc);
+  reconstruct_rows<KDA, BITS, FIT, WW>(p, n, L, sm, acc);
   const Tail tl = carve_tail(sm, p.r1);
   keep_factors<FIT>(p, tl);
   __syncthreads();  // every staged input has been read: the tile may overwrite them
