@@ -76,14 +76,6 @@ __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
   return d;
 }
 
-// Exact int8 -> fp32 of bytes b and b' of two biased words, as one pair.
-__device__ __forceinline__ f32x2 code_pair(uint32_t w_lo, int b_lo, uint32_t w_hi, int b_hi) {
-  const f32x2 bias = f2_pack(8388736.0f, 8388736.0f);
-  return f2_sub(f2_bits(__byte_perm(w_lo, 0x4B000000u, 0x7540u | (uint32_t)b_lo),
-                        __byte_perm(w_hi, 0x4B000000u, 0x7540u | (uint32_t)b_hi)),
-                bias);
-}
-
 // A lane's 16 codes of one row as four words of biased bytes, and the exact
 // conversion of code e (0..15) from them. Row layouts (one row = d_k codes):
 //  8-bit (128 B): int8 codes; lane qq's block is bytes 16qq..16qq+15, and the
@@ -579,10 +571,36 @@ static int smem_of(const Params& q, bool tile) { return tile ? q.r1 + kTailBytes
 
 template <typename K>
 static cudaError_t set_smem(K kernel, int smem) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // The attributes are set once per kernel and device on each thread, and
+  // again only when a launch needs more dynamic shared memory than was allowed
+  // so far: two cudaFuncSetAttribute calls per launch were host time on every
+  // decode step. A small per-thread table remembers what was set.
+  struct Seen {
+    const void* fn;
+    int dev;
+    int smem;
+  };
+  constexpr int kSeen = 32;
+  thread_local Seen seen[kSeen] = {};
+  thread_local int next = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int at = -1;
+  for (int t = 0; t < kSeen; ++t)
+    if (seen[t].fn == fn && seen[t].dev == dev) at = t;
+  if (at >= 0 && seen[at].smem >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  return e;
+  if (e != cudaSuccess) return e;
+  if (at < 0) {
+    at = next;
+    next = (next + 1) % kSeen;
+  }
+  seen[at] = Seen{fn, dev, smem};
+  return cudaSuccess;
 }
 
 // One CTA per head-state (grid = p.n_states), or `grid` CTAs.
