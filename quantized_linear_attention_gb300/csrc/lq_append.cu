@@ -41,8 +41,8 @@
 
 namespace lqi {
 
-// Thread 0: barrier init, the record count (read first only when the phase is
-// not stated) and the bulk copies of what the matvec and the row pass read --
+// Thread 0: barrier init, the record count and the header (read first) and the
+// bulk copies of what the matvec and the row pass read --
 // the codes, the compensator ids and lines, the record corrections -- then,
 // with scalar decay, the decay chain P_n = 1, P_{m-1} = P_m alpha_m from the
 // held records' decays (loaded first thing) into the P table, while the copies
@@ -53,12 +53,29 @@ __device__ __forceinline__ StageInfo append_start(const Params& p, int64_t s, in
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     const Stage& L = p.st;
-    int n0 = known, c = 0, h = 0;
-    if (n0 < 0) {
-      c = p.counts[s];
-      h = header_ok(p) ? 1 : 0;
-      n0 = (h && c >= 0 && c <= max_n0) ? c : -1;
-    }
+    // the record count and the header are read first; with a stated phase
+    // nothing waits for them until the end, so their latency overlaps the rest
+    const int c = p.counts[s];
+    const int h = header_ok(p) ? 1 : 0;
+    // the held decays (scalar decay), read before the first product so that the
+    // chain runs at multiply latency; with a stated phase, before the copies
+    float al[WMAX];
+    auto load_decays = [&](int n_held) {
+      const float4* a4 = reinterpret_cast<const float4*>(p.rec_alpha + s * p.alpha_stride);
+#pragma unroll
+      for (int q4 = 0; q4 < WMAX / 4; ++q4) {
+        if (4 * q4 < n_held) {
+          const float4 x = a4[q4];
+          al[4 * q4] = x.x;
+          al[4 * q4 + 1] = x.y;
+          al[4 * q4 + 2] = x.z;
+          al[4 * q4 + 3] = x.w;
+        }
+      }
+    };
+    if (!KDA && known >= 0) load_decays(known);
+    int n0 = known;
+    if (n0 < 0) n0 = (h && c >= 0 && c <= max_n0) ? c : -1;
     if (n0 >= 0) {
       const uint32_t code_bytes = (uint32_t)(kD * kD * p.bits / 8);
       const uint32_t comp_floats = (uint32_t)(kD * C * (p.comp_fit > 0 ? 2 : 1));
@@ -72,20 +89,7 @@ __device__ __forceinline__ StageInfo append_start(const Params& p, int64_t s, in
       if (C > 0) bulk_g2s(sm + L.comp_line, p.comp_line + s * comp_floats, 4u * comp_floats, bar);
       if (n0 > 0) bulk_g2s(sm + L.rec_u, p.rec_u + s * W * kD, rec, bar);
       if (!KDA) {
-        // every held decay is read before the first product, so the chain runs
-        // at multiply latency
-        float al[WMAX];
-        const float4* a4 = reinterpret_cast<const float4*>(p.rec_alpha + s * p.alpha_stride);
-#pragma unroll
-        for (int q4 = 0; q4 < WMAX / 4; ++q4) {
-          if (4 * q4 < n0) {
-            const float4 x = a4[q4];
-            al[4 * q4] = x.x;
-            al[4 * q4 + 1] = x.y;
-            al[4 * q4 + 2] = x.z;
-            al[4 * q4 + 3] = x.w;
-          }
-        }
+        if (known < 0) load_decays(n0);
         const int n = n0 + 1;
         float pr = 1.0f;
         P[n] = pr;
@@ -99,10 +103,6 @@ __device__ __forceinline__ StageInfo append_start(const Params& p, int64_t s, in
           }
         }
       }
-    }
-    if (known >= 0) {
-      c = p.counts[s];
-      h = header_ok(p) ? 1 : 0;
     }
     sh->issued = n0;
     sh->cnt = c;

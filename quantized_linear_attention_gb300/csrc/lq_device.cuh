@@ -31,8 +31,12 @@ extern __shared__ __align__(128) char lq_dyn_smem[];
 // small device helpers
 
 __device__ __forceinline__ bool header_ok(const Params& p) {
+  // all three loads are issued before any comparison (one round trip, not three)
   const Header* h = p.hdr;
-  return h->magic == kMagic && h->cfg_hash == p.cfg_hash && h->n_states == p.n_states;
+  const auto magic = h->magic;
+  const auto hash = h->cfg_hash;
+  const auto n = h->n_states;
+  return (magic == kMagic) & (hash == p.cfg_hash) & (n == p.n_states);
 }
 
 __device__ __forceinline__ void set_error(const Params& p, int code, int64_t s) {
@@ -301,6 +305,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// Orders this thread's earlier shared-memory accesses (generic proxy) before
+// its later bulk copies into the same bytes (async proxy).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // memory into this CTA's shared memory; completion is counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -485,7 +493,10 @@ __device__ __forceinline__ StageInfo stage_start(const Params& p, int64_t s, int
                                                  uint64_t* bar, StageInfo* sh, bool stage_k, int max_n0,
                                                  bool init_bar = true, bool stage_a = true) {
   if (threadIdx.x == 0) {
-    if (init_bar) mbar_init(bar, 1);
+    if (init_bar)
+      mbar_init(bar, 1);
+    else
+      fence_proxy_async();  // the staging area is reused: what this CTA read and wrote there comes first
     int n0 = known_n0;
     if (n0 >= 0) stage_issue(p, s, n0, L, lq_dyn_smem, bar, stage_k, stage_a);
     const int c = p.counts[s];
@@ -609,6 +620,22 @@ static cudaError_t launch(K kernel, const Params& p, int smem, cudaStream_t st, 
   const cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
   kernel<<<dim3((unsigned)(grid >= 0 ? grid : p.n_states)), dim3(threads), (size_t)smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// As many CTAs as fit on the GPU at once (never more than head-states), for
+// kernels whose CTAs walk the head-states.
+template <typename K>
+static cudaError_t launch_resident(K kernel, const Params& p, int smem, cudaStream_t st, int threads) {
+  cudaError_t e = set_smem(kernel, smem);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > p.n_states) grid = p.n_states;
+  kernel<<<dim3((unsigned)grid), dim3(threads), (size_t)smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -766,8 +766,8 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
 
   // F2: C greedy rounds of the longest line, ties to the smallest id. Warp 0
   // finds the winner from this round's scores (lane L scans ids L, L+32, ...
-  // in ascending order, then a butterfly keeps the larger score, the smaller
-  // id on a tie) and publishes it. The next round's scores go to the other
+  // in ascending order and keeps its first largest; two warp reductions then
+  // give the largest score and the smallest id holding it) and publishes it. The next round's scores go to the other
   // score array, so nothing a round reads is written during it. Then, in
   // parallel:
   //  - threads 0..127 refresh the scores the taken line changes: taking row i*
@@ -795,16 +795,11 @@ __device__ __forceinline__ void boundary_from_tile(const Params& p, int64_t s, f
           bi = L + 32 * e;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bsc, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bsc || (ov == bsc && oi < bi)) {
-          bsc = ov;
-          bi = oi;
-        }
-      }
-      if (L == 0) s_win = bi;
+      // The warp's largest score (non-negative floats order as their bit
+      // patterns), then the smallest id among the lanes that hold it.
+      const uint32_t top = __reduce_max_sync(0xffffffffu, __float_as_uint(bsc));
+      const uint32_t wid = __reduce_min_sync(0xffffffffu, __float_as_uint(bsc) == top ? (uint32_t)bi : 0xffffffffu);
+      if (L == 0) s_win = (int)wid;
     }
     __syncthreads();
     const int win = s_win;

@@ -902,17 +902,7 @@ cudaError_t launch_fold(const Params& p, cudaStream_t st) {
 // As many CTAs as fit on the GPU at once (never more than head-states).
 template <typename K>
 static cudaError_t launch_listed(K kernel, const Params& q, cudaStream_t st) {
-  const int smem = smem_of(q, true);
-  cudaError_t e = set_smem(kernel, smem);
-  int dev = 0, sms = 0, per_sm = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, (size_t)smem);
-  if (e != cudaSuccess) return e;
-  int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
-  if (grid > q.n_states) grid = q.n_states;
-  kernel<<<dim3((unsigned)grid), dim3(256), (size_t)smem, st>>>(q);
-  return cudaGetLastError();
+  return launch_resident(kernel, q, smem_of(q, true), st, 256);
 }
 
 cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
