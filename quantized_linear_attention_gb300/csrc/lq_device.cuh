@@ -163,6 +163,19 @@ __device__ __forceinline__ void code_quad(const uint32_t (&cw)[4], int e0, f32x2
   }
 }
 
+// 4- and 6-bit codes: the pair of columns (e, e + 1), e even, of a block as
+// code_words gives it (element e at byte (e & 7) / 2 of word 2 (e / 8), element
+// e + 1 at the same byte of the next word), converted exactly as code_quad does.
+template <int BITS>
+__device__ __forceinline__ f32x2 code_cols(const uint32_t (&cw)[4], int e) {
+  static_assert(BITS == 4 || BITS == 6, "8-bit columns pair up in code_quad");
+  constexpr float bias = BITS == 6 ? 8388640.0f : 8388616.0f;
+  const uint32_t we = cw[2 * (e >> 3)], wo = cw[2 * (e >> 3) + 1];
+  const uint32_t b = (uint32_t)((e & 7) >> 1);
+  return f2_sub(f2_bits(__byte_perm(we, 0x4B000000u, 0x7540u | b), __byte_perm(wo, 0x4B000000u, 0x7540u | b)),
+                f2_pack(bias, bias));
+}
+
 // f in both halves of a pair: the packed fma takes it as a broadcast operand.
 __device__ __forceinline__ f32x2 f2_dup(float f) { return f2_pack(f, f); }
 

@@ -146,9 +146,9 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
   f32x2 a2[4][8];
   {
     // The base: ((sigma_i Cd_ij) lambda_j) P_0[j], three products in this order
-    // (multiplies only, so nothing can be contracted). With 8-bit codes the
-    // conversion gives the pairs (2k, 2k+1) directly and the products run in
-    // packed pairs, sigma_i broadcast; other widths multiply per element.
+    // (multiplies only, so nothing can be contracted). The conversion gives the
+    // column pairs (2k, 2k+1) directly and the products run in packed pairs,
+    // sigma_i broadcast.
     const float* lam = at<float>(sm, L.lam_b) + 20 * qq;
     const float* p0b = P_b + 20 * qq;
     const int8_t* cb = at<int8_t>(sm, L.codes);
@@ -158,7 +158,7 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
       const float s_i = sg[i];
       uint32_t cw[4];
       code_words<BITS>(cb + i * row_bytes<BITS>(), qq, cw);
-      if (BITS == 8) {
+      if constexpr (BITS == 8) {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           f32x2 f01, f23;
@@ -174,15 +174,14 @@ __device__ __forceinline__ void reconstruct_rows(const Params& p, int n, const S
           a2[pp][2 * c4 + 1] = f2_mul(f2_mul(f2_mul(f2_pack(s_i, s_i), f23), l2.y), q2.y);
         }
       } else {
-        float f[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) f[t] = code_at<BITS>(cw, t);
+        // 4- and 6-bit codes: columns 2k and 2k + 1 sit at the same byte of the
+        // even and the odd word, so they convert as one pair too
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float2 l2 = *reinterpret_cast<const float2*>(lam + 2 * k);
-          const float2 q2 = KDA ? *reinterpret_cast<const float2*>(p0b + 2 * k) : make_float2(P[0], P[0]);
-          a2[pp][k] = f2_pack(__fmul_rn(__fmul_rn(__fmul_rn(s_i, f[2 * k]), l2.x), q2.x),
-                              __fmul_rn(__fmul_rn(__fmul_rn(s_i, f[2 * k + 1]), l2.y), q2.y));
+          const f32x2 f01 = code_cols<BITS>(cw, 2 * k);
+          const f32x2 l2 = *reinterpret_cast<const f32x2*>(lam + 2 * k);
+          const f32x2 q2 = KDA ? *reinterpret_cast<const f32x2*>(p0b + 2 * k) : f2_pack(P[0], P[0]);
+          a2[pp][k] = f2_mul(f2_mul(f2_mul(f2_pack(s_i, s_i), f01), l2), q2);
         }
       }
     }
