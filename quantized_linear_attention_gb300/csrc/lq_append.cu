@@ -120,8 +120,8 @@ __device__ __forceinline__ StageInfo append_start(const Params& p, int64_t s, in
 // n = records after this token (n0 held + 1). CC, WW: the compensator count
 // and window length when fixed at compile time (the pages' configuration,
 // C = 4 and W = 16, has its own instantiation), 0 when read from p.
-template <bool KDA, int BITS, bool FIT, bool SLIST = false, int CC = 0, int WW = 0>
-__global__ void __launch_bounds__(128, KDA ? 5 : 8) k_append(Params p) {
+template <bool KDA, int BITS, bool FIT, bool SLIST = false, int CC = 0, int WW = 0, int MINB = 8>
+__global__ void __launch_bounds__(128, KDA ? 5 : MINB) k_append(Params p) {
   constexpr int CMAX = CC ? CC : kMaxC;
   constexpr int WMAX = WW ? WW : kMaxW;
   const int C = CC ? CC : p.C;
@@ -279,7 +279,14 @@ static Params append_params(const Params& p) {
 cudaError_t launch_append(const Params& p, cudaStream_t st) {
   const Params q = append_params(p);
   if (q.C == 4 && q.W == 16 && q.comp_fit == 0) {
-    // the pages' configuration, with C and W fixed at compile time
+    // the pages' configuration, with C and W fixed at compile time. With scalar
+    // decay and few records staged, 9 CTAs fit on an SM by shared memory (228 KB,
+    // 1 KB reserved per CTA): those launches take the build limited to 56
+    // registers, which fits 9 by registers too (6-bit codes spill there).
+    if (!q.kda && q.bits != 6 && 9 * (q.st.end + 1024 + 256) <= 228 * 1024) {
+      auto k9 = q.bits == 4 ? k_append<false, 4, false, false, 4, 16, 9> : k_append<false, 8, false, false, 4, 16, 9>;
+      return launch(k9, q, q.st.end, st, 128);
+    }
     auto k = q.kda ? (q.bits == 4 ? k_append<true, 4, false, false, 4, 16>
                                   : (q.bits == 6 ? k_append<true, 6, false, false, 4, 16>
                                                  : k_append<true, 8, false, false, 4, 16>))
