@@ -26,3 +26,18 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "gdn-tiny-1x2"
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches N > 1 (torch.distributed.run, two ranks on
+    127.0.0.1): rank 0 alone runs the oracle and prints the line; rank 1 exits 0."""
+    env = dict(os.environ, LQ_REFERENCE_BUDGET_S="2")
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                          "--master-addr", "127.0.0.1", "--master-port", "29517", "bench.py", "--impl", "reference",
+                          "--gpus", "2", "--workload", "1", "--steps", "1", "--warmup", "3"],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [line for line in out.stdout.splitlines() if line.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["value"] > 0
