@@ -187,37 +187,6 @@ __device__ __forceinline__ float tree8(float x) {
   return x;
 }
 
-__device__ __forceinline__ float max8(float x) {
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-  return x;
-}
-
-// Eight quantities at once: v[k] is this lane's block partial of quantity k.
-// Three exchange-and-add steps leave lane qq of the group with the full tree
-// ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)) of quantity 4*(qq&1) + 2*((qq>>1)&1) +
-// ((qq>>2)&1): the same additions as tree8, in the same order, shared out.
-__device__ __forceinline__ float tree8_transpose(const float v[8], int qq) {
-  const bool b0 = (qq & 1) != 0, b1 = (qq & 2) != 0, b2 = (qq & 4) != 0;
-  float s4[4], s2[2];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float keep = b0 ? v[4 + k] : v[k];
-    const float send = b0 ? v[k] : v[4 + k];
-    s4[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float keep = b1 ? s4[2 + k] : s4[k];
-    const float send = b1 ? s4[k] : s4[2 + k];
-    s2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  }
-  const float keep = b2 ? s2[1] : s2[0];
-  const float send = b2 ? s2[0] : s2[1];
-  return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-}
-
 // Q quantities (Q = 8 or 16) at once: v[k] is this lane's block partial of
 // quantity k. Three exchange-and-add steps (partners lane^1, ^2, ^4) leave lane
 // qq with the full trees of quantities (Q/2)b0 + (Q/4)b1 + (Q/8)b2 + e,

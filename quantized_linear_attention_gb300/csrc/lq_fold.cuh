@@ -46,24 +46,6 @@ __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, co
   }
 }
 
-// P_m over the 16-element block qq of a lane: GDN broadcasts one scalar.
-template <bool KDA>
-__device__ __forceinline__ void decay_block(const float* P, const float* P_b, int m, int qq, float d[16]) {
-  if (KDA) {
-    load16(P_b + m * kBV + 20 * qq, d);
-  } else {
-    const float x = P[m];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) d[t] = x;
-  }
-}
-
-template <bool KDA>
-__device__ __forceinline__ float decay_at(const float* P, const float* P_b, int m, int j) {
-  return KDA ? P_b[m * kBV + bv(j)] : P[m];
-}
-
-
 // ---------------------------------------------------------------------------
 // Fold (F0-F6). LeapQuant App. B.3: the state is reconstructed in original
 // coordinates at the window boundary; §3.3: compensators are the largest
@@ -326,20 +308,6 @@ __device__ __forceinline__ void tile_store_rows(float* S, const Tail& tl, float 
           make_float4(acc[pp][4 * c4], acc[pp][4 * c4 + 1], acc[pp][4 * c4 + 2], acc[pp][4 * c4 + 3]);
   }
   __syncthreads();
-}
-
-// Column block chain: fma (squares) or add (absolute values) over rows
-// 16b..16b+15 of column j, ascending (coff from column_offsets(j)).
-template <bool SQUARES>
-__device__ __forceinline__ float column_block(const float* S, int b, const int coff[8]) {
-  const float* base = S + 16 * b * kD;
-  float x[16];
-#pragma unroll
-  for (int t = 0; t < 16; ++t) x[t] = base[t * kD + coff[t & 7]];
-  float acc = 0.0f;
-#pragma unroll
-  for (int t = 0; t < 16; ++t) acc = SQUARES ? __fmaf_rn(x[t], x[t], acc) : __fadd_rn(acc, fabsf(x[t]));
-  return acc;
 }
 
 // Block partials of every column (SQUARES: fma chains of squares; else add
