@@ -38,8 +38,10 @@
  *     another configuration) set the state buffer's status word, which
  *     lq_get_status reads; the affected head-states are left unchanged.
  *   - Threads: no global mutable state except a thread-local error message,
- *     the thread-local test hook of lq_debug_set_wait, and the device address
- *     of lq_decode_step_noalloc's fixed array, looked up once per device.
+ *     the thread-local test hook of lq_debug_set_wait, a thread-local record
+ *     of the kernel attributes (shared-memory size) already set per kernel and
+ *     device, and the device address of lq_decode_step_noalloc's fixed array,
+ *     looked up once per device.
  *   - n_states = 0 is valid and does nothing.
  */
 #ifndef LQ_H
