@@ -156,7 +156,8 @@ def profile_traffic(n_states, summary=PROFILE_SUMMARY):
         cap = int(fields["captured_head_states"])
     except (KeyError, ValueError):
         return None, "summary lacks dram_bytes_per_launch / captured_head_states"
-    return round(per * n_states / cap), f"ncu capture at {cap} head-states, phase-averaged, scaled to {n_states}"
+    how = "phase-averaged, " if summary == PROFILE_SUMMARY else ""
+    return round(per * n_states / cap), f"ncu capture at {cap} head-states, {how}scaled to {n_states}"
 
 
 class ClockSampler:
