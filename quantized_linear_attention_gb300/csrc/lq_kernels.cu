@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(128, 4) k_append_rwkv(Params p) {
 
 // Fold with the records held (any count 0..W): lq_fold.
 template <bool KDA, int BITS, bool FIT>
-__global__ void __launch_bounds__(256, 3) k_fold(Params p) {
+__global__ void __launch_bounds__(256, FIT ? 2 : 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(256, 3) k_fold(Params p) {
 // so the few head-states whose window fills this token are spread over every
 // SM. Each entry must hold W records. The last CTA to finish empties the list.
 template <bool KDA, int BITS, bool FIT, bool SLIST = false>
-__global__ void __launch_bounds__(256, 3) k_fold_listed(Params p) {
+__global__ void __launch_bounds__(256, FIT ? 2 : 3) k_fold_listed(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   __shared__ int s_nfull;
@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(256, 3) k_export(Params p) {
 // writes the header. A range (p.first >= 0): block b re-initialises head-state
 // first + b from S0 row block b, and the header must already match.
 template <int BITS, bool FIT>
-__global__ void __launch_bounds__(256, 3) k_init(Params p) {
+__global__ void __launch_bounds__(256, FIT ? 2 : 3) k_init(Params p) {
   __shared__ int s_ok;
   const bool range = p.first >= 0;
   const int64_t s = (range ? p.first : 0) + blockIdx.x;

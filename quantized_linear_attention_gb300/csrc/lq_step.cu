@@ -31,7 +31,7 @@ __device__ __forceinline__ void append_bar() { asm volatile("bar.sync 1, 128;" :
 // (the pages' configuration, C = 4 and W = 16, has its own instantiation), 0
 // when read from p.
 template <bool KDA, int BITS, bool FIT, int CC = 0, int WW = 0>
-__global__ void __launch_bounds__(256, 3) k_step(Params p) {
+__global__ void __launch_bounds__(256, FIT ? 2 : 3) k_step(Params p) {
   constexpr int CMAX = CC ? CC : kMaxC;
   constexpr int WMAX = WW ? WW : kMaxW;
   const int C = CC ? CC : p.C;
