@@ -777,7 +777,7 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_fold_listed(Params p) {
 
 // The state each head-state stands for (F0-F1, no rounding): lq_export_state.
 template <bool KDA, int BITS, bool FIT>
-__global__ void __launch_bounds__(256, 3) k_export(Params p) {
+__global__ void __launch_bounds__(256, FIT ? 2 : 3) k_export(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
