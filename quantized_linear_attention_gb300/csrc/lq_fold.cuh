@@ -15,10 +15,13 @@ namespace lqi {
 
 
 
-// Decay products from staged alphas (records 1..n-1, then alpha_n = the current
-// token's, or records 1..n when have_cur is false). Backward running products,
-// no division: P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.
-// GDN: scalars P[m] (thread 0). KDA: blocked rows P_b[m] (threads 0..127).
+// Decay products from the records' alphas (records 1..n-1, then alpha_n = the
+// current token's, or records 1..n when have_cur is false). Backward running
+// products, no division: P_n = 1, P_{m-1} = P_m * alpha_m for m = n..1.
+// GDN: scalars P[m] (thread 0), from the staged alphas. KDA: blocked rows P_b[m]
+// (threads 0..127, thread j the column j), from the head-state's alphas in
+// global memory (they are not staged, so that the fold's staging fits in the
+// state tile's space), sixteen loads issued before their products.
 template <bool KDA>
 __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, const float* cur_vec, float cur_scalar,
                                                bool have_cur, float* P, float* P_b) {
@@ -28,10 +31,21 @@ __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, co
       const int jb = bv(tid);
       float pr = 1.0f;
       P_b[n * kBV + jb] = pr;
-      for (int m = n; m >= 1; --m) {
-        const float am = (have_cur && m == n) ? cur_vec[tid] : rec_alpha[(m - 1) * kD + tid];
-        pr = __fmul_rn(pr, am);
-        P_b[(m - 1) * kBV + jb] = pr;
+      for (int mh = n; mh >= 1; mh -= 16) {
+        float am[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int m = mh - e;
+          if (m >= 1) am[e] = (have_cur && m == n) ? cur_vec[tid] : rec_alpha[(m - 1) * kD + tid];
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int m = mh - e;
+          if (m >= 1) {
+            pr = __fmul_rn(pr, am[e]);
+            P_b[(m - 1) * kBV + jb] = pr;
+          }
+        }
       }
     }
   } else if (tid == 0) {
@@ -957,8 +971,8 @@ __device__ __forceinline__ void keep_factors(const Params& p, const Tail& tl) {
 template <bool KDA, int BITS, bool FIT>
 __device__ __forceinline__ void fold_staged(const Params& p, int64_t s, int n) {
   const Stage& L = p.st;
-  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
-                      at<float>(lq_dyn_smem, L.P_b));
+  decay_products<KDA>(n, KDA ? p.rec_alpha + s * p.alpha_stride : at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f,
+                      false, at<float>(lq_dyn_smem, L.P), at<float>(lq_dyn_smem, L.P_b));
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];

@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_fold(Params p) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ StageInfo s_info;
   const int64_t s = blockIdx.x;
-  const StageInfo si = stage_start(p, s, -1, p.st, &bar, &s_info, true, p.W);
+  const StageInfo si = stage_start(p, s, -1, p.st, &bar, &s_info, true, p.W, true, !KDA);
   const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
   fold_staged<KDA, BITS, FIT>(p, s, n);
@@ -753,7 +753,8 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_fold_listed(Params p) {
       if (threadIdx.x == 0) set_error(p, LQ_ERR_STATE, s);
       continue;
     }
-    const StageInfo si = stage_start(p, s, p.W, p.st, &bar, &s_info, true, p.W, parity == 0 && t == blockIdx.x);
+    const StageInfo si =
+        stage_start(p, s, p.W, p.st, &bar, &s_info, true, p.W, parity == 0 && t == blockIdx.x, !KDA);
     const int n = stage_finish(p, s, &bar, si, false, parity);
     parity ^= 1u;
     if (n == -2) break;  // copies may still land: the barrier is not reused
@@ -784,11 +785,11 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_export(Params p) {
   const int tid = threadIdx.x;
   const int w = tid >> 5, r = (tid & 31) >> 3, qq = tid & 7;
   const Stage& L = p.st;
-  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, true, p.W);
+  const StageInfo si = stage_start(p, s, -1, L, &bar, &s_info, true, p.W, true, !KDA);
   const int n = stage_finish(p, s, &bar, si, false);
   if (n < 0) return;
-  decay_products<KDA>(n, at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f, false, at<float>(lq_dyn_smem, L.P),
-                      at<float>(lq_dyn_smem, L.P_b));
+  decay_products<KDA>(n, KDA ? p.rec_alpha + s * p.alpha_stride : at<float>(lq_dyn_smem, L.rec_alpha), nullptr, 0.0f,
+                      false, at<float>(lq_dyn_smem, L.P), at<float>(lq_dyn_smem, L.P_b));
   __syncthreads();
   fold_tables<KDA>(p, n, L, lq_dyn_smem);
   float acc[4][16];
@@ -895,7 +896,7 @@ cudaError_t launch_append_rwkv(const Params& p, cudaStream_t st) {
 #undef LQ_PICK_R
 
 cudaError_t launch_fold(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  const Params q = with_layout(p, p.W, p.W, false, true, true, false, false, !p.kda);
   return launch(LQ_PICK2(k_fold, q), q, smem_of(q, true), st);
 }
 
@@ -906,7 +907,7 @@ static cudaError_t launch_listed(K kernel, const Params& q, cudaStream_t st) {
 }
 
 cudaError_t launch_fold_listed(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  const Params q = with_layout(p, p.W, p.W, false, true, true, false, false, !p.kda);
   return launch_listed(LQ_PICK2(k_fold_listed, q), q, st);
 }
 
@@ -952,13 +953,13 @@ cudaError_t launch_decode_noalloc(const Params& p, int dev, cudaStream_t st) {
   r.full_list = scratch + kNoAllocListOffset;
   e = launch_append_slist(r, st);
   if (e != cudaSuccess) return e;
-  const Params f = with_layout(r, r.W, r.W, false, true, true);
+  const Params f = with_layout(r, r.W, r.W, false, true, true, false, false, !r.kda);
   return f.kda ? launch_listed(k_fold_listed<true, 8, false, true>, f, st)
                : launch_listed(k_fold_listed<false, 8, false, true>, f, st);
 }
 
 cudaError_t launch_export(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, p.W, p.W, false, true, true);
+  const Params q = with_layout(p, p.W, p.W, false, true, true, false, false, !p.kda);
   return launch(LQ_PICK2(k_export, q), q, smem_of(q, true), st);
 }
 

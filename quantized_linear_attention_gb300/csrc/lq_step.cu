@@ -64,13 +64,14 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_step(Params p) {
       q4 = reinterpret_cast<const float4*>(p.q + s * kD)[tid & 31];
     }
   }
-  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, W - 1);
+  const StageInfo si = stage_start(p, s, known, L, &bar, &s_info, true, W - 1, true, !KDA);
   const int n0 = stage_finish(p, s, &bar, si, true);
   if (n0 < 0) return;
   const int n = n0 + 1;  // == W: the phase was stated as W - 1 and checked
 
   // A0: decay products over the held records and this token's decay.
-  decay_products<KDA>(n, at<float>(sm, L.rec_alpha), p.alpha + s * kD, alpha_s, true, a.P(), a.P_b());
+  decay_products<KDA>(n, KDA ? p.rec_alpha + s * p.alpha_stride : at<float>(sm, L.rec_alpha), p.alpha + s * kD, alpha_s,
+                      true, a.P(), a.P_b());
   __syncthreads();
 
   float* kd_b = at<float>(sm, L.kd_b);
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_step(Params p) {
 #define LQ_PICK2(K, q) ((q).kda ? LQ_PICK_B(K, q, true) : LQ_PICK_B(K, q, false))
 
 cudaError_t launch_step(const Params& p, cudaStream_t st) {
-  const Params q = with_layout(p, p.W, p.W, true, true, true);
+  const Params q = with_layout(p, p.W, p.W, true, true, true, false, false, !p.kda);
   if (q.C == 4 && q.W == 16 && q.comp_fit == 0) {
     // the pages' configuration, with C and W fixed at compile time
     auto k = q.kda ? (q.bits == 4 ? k_step<true, 4, false, 4, 16>
