@@ -60,6 +60,32 @@ __device__ __forceinline__ void decay_products(int n, const float* rec_alpha, co
   }
 }
 
+// The same per-key chain (KDA, threads 0..127) with this token's decay a_cur as
+// record n's and the first NPRE held records' decays already in registers
+// (read before the staging wait); records beyond NPRE come from global memory.
+template <int NPRE>
+__device__ __forceinline__ void kda_decay_regs(const Params& p, int64_t s, int n, float a_cur,
+                                               const float (&apre)[NPRE], float* P_b) {
+  const int tid = threadIdx.x;
+  if (tid >= kD) return;
+  const int jb = bv(tid);
+  float pr = 1.0f;
+  P_b[n * kBV + jb] = pr;
+  pr = __fmul_rn(pr, a_cur);
+  P_b[(n - 1) * kBV + jb] = pr;
+  for (int m = n - 1; m > NPRE; --m) {
+    pr = __fmul_rn(pr, p.rec_alpha[s * p.alpha_stride + (m - 1) * kD + tid]);
+    P_b[(m - 1) * kBV + jb] = pr;
+  }
+#pragma unroll
+  for (int m = NPRE; m >= 1; --m) {
+    if (m <= n - 1) {
+      pr = __fmul_rn(pr, apre[m - 1]);
+      P_b[(m - 1) * kBV + jb] = pr;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Fold (F0-F6). LeapQuant App. B.3: the state is reconstructed in original
 // coordinates at the window boundary; §3.3: compensators are the largest

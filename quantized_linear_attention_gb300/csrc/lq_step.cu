@@ -53,12 +53,16 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_step(Params p) {
   const float beta = p.beta[s];
   float kj = 0.0f, qj = 0.0f, vi = 0.0f, lamj = 0.0f, aj = 0.0f;
   float4 k4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), q4 = k4;
+  float apre[kAPre];  // per-key decay: column tid of the held records' decays
   if (tid < kD) {
     kj = p.k[s * kD + tid];
     qj = p.q[s * kD + tid];
     vi = p.v[s * kD + irow];
     lamj = p.lambda[s * kD + tid];
-    if (KDA) aj = p.alpha[s * kD + tid];
+    if (KDA) {
+      aj = p.alpha[s * kD + tid];
+      prefetch_alpha(p, s, W - 1, apre);
+    }
     if (w == 3) {
       k4 = reinterpret_cast<const float4*>(p.k + s * kD)[tid & 31];
       q4 = reinterpret_cast<const float4*>(p.q + s * kD)[tid & 31];
@@ -70,8 +74,10 @@ __global__ void __launch_bounds__(256, FIT ? 2 : 3) k_step(Params p) {
   const int n = n0 + 1;  // == W: the phase was stated as W - 1 and checked
 
   // A0: decay products over the held records and this token's decay.
-  decay_products<KDA>(n, KDA ? p.rec_alpha + s * p.alpha_stride : at<float>(sm, L.rec_alpha), p.alpha + s * kD, alpha_s,
-                      true, a.P(), a.P_b());
+  if constexpr (KDA)
+    kda_decay_regs<kAPre>(p, s, n, aj, apre, a.P_b());
+  else
+    decay_products<false>(n, at<float>(sm, L.rec_alpha), nullptr, alpha_s, true, a.P(), nullptr);
   __syncthreads();
 
   float* kd_b = at<float>(sm, L.kd_b);
