@@ -570,9 +570,9 @@ def time_e2e(wl, steps, device, ring=8):
     decode calls, as a serving loop would: host-to-device for token t+1 while
     token t decodes, device-to-host of each output once its token is done
     (a ring of `ring` token slots on the device, ordered by events). A token's
-    inputs take longer to copy (about 120 us at 210 GB/s) than its append takes
-    to run (106 us), so the copies must run ahead through the window's fold
-    token: 8 slots let them, 4 did not (95 M against 108 M head-tokens/s)."""
+    inputs take longer to copy (about 125 us at 205 GB/s) than its append takes
+    to run (90 us), so the copies must run ahead through the window's fold
+    token: 8 slots let them, 4 did not."""
     import torch
 
     from quantized_linear_attention_gb300 import lq
