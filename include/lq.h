@@ -300,8 +300,8 @@ int lq_export_state(const lq_config* cfg, const void* state, int64_t n_states, f
 
 /*
  * The fp32-state baseline: one decode token of the plain delta rule on whole
- * fp32 states, the "FP32 kernel" that LeapQuant's kernel speedups are measured
- * against ([LQ] §4.3; the update is §3.1 and App. A):
+ * fp32 states: the kind of fp32-state kernel that LeapQuant's kernel speedups
+ * are measured against ([LQ] §4.3; the update is §3.1 and App. A):
  *   u = beta (v - S (alpha . k)),  S <- S Diag(alpha) + u k^T,  o = S q.
  * S: fp32 [n_states][d_v][d_k] on the device, read and written in place (it is
  * not an lq state buffer: no header, codes or records). Token arguments as

@@ -60,7 +60,8 @@ typedef struct {
   int32_t comp_fit;      /* 0: compensators are outlier lines (id + line);       */
                          /* s > 0: rank-one factors (a, b) fitted by s sweeps of */
                          /* power iteration from the longest row ([RN4] "Where   */
-                         /* the time goes"; [LQ] App. B.3 "fitting new factors") */
+                         /* the time goes"; [LQ] App. B.3: factors refitted at   */
+                         /* the boundary)                                        */
   int32_t comp_block;    /* with comp_fit > 0: 1 fits the C factors together as  */
                          /* a block from the previous window's factors ([RN4]    */
                          /* "Redesign"); 0 one at a time as above                */
@@ -344,7 +345,7 @@ static void normalize(int d, float* b) {
 /*
  * F2, fitted-factor reading of the compensators ([LQ] §3.3: dominant state
  * components kept as high-precision rank-one terms; App. B.3: the state is
- * reconstructed "before fitting new factors"; [RN4] "Where the time goes": four
+ * rebuilt first and the new factors fitted on it; [RN4] "Where the time goes": four
  * compensators found one at a time, eight sweeps each, starting from the
  * longest row). For c = 0..C-1, on the residual R:
  *   b = the longest row of R (largest squared length, ties to the smallest index);
@@ -555,8 +556,9 @@ static void boundary_from_state(const orc_cfg* cfg, const float* S, orc_view st,
 
 /*
  * F0-F1: the state at the end of the records, in original coordinates
- * ([LQ] App. B.3: reconstructed before fitting new factors and recomputing the
- * residual scales; [LQ] §3.3: compensators are records at window position 0):
+ * ([LQ] App. B.3: the state is rebuilt at the boundary, then the factors and
+ * the residual's scales are computed anew; [LQ] §3.3: compensators are records
+ * at window position 0):
  *   S_ij = ((sigma_i * Cd_ij) * lambda_j) * P_0[j]
  *          then fma(a_c[i], (P_0 . b_c)[j], .) for c = 0..C-1
  *          then fma(u_m[i], (P_m . k_m)[j], .) for m = 1..n.

@@ -1,5 +1,5 @@
 """Pins of the fitted-factor reading of the compensators (LeapQuant §3.3 dominant
-state components as rank-one terms; App. B.3 "fitting new factors"; research
+state components as rank-one terms; App. B.3, factors refitted at the boundary; research
 note 4: eight power-iteration sweeps per compensator from the longest row),
 against results the oracle does not compute itself."""
 import numpy as np
