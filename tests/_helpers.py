@@ -69,3 +69,28 @@ def tie_rows(qm):
         S0[0, r, :len(base)] = np.float32(2.0 ** (r - 1)) * np.asarray(base, np.float32)
         codes[0, r, :len(want)] = want
     return S0, codes
+
+
+def selection_ties():
+    """States whose compensator selection (C = 4) meets exact score ties, with the ids
+    the tie rule gives (reading R5: largest squared length, ties to the smallest id, rows
+    0..127 before columns 128..255), worked out by hand:
+    - a constant state: every line has the same length; taking row 0 shortens every
+      column by one entry, so rows 1, 2, 3 follow;
+    - row 5 and column 9 all ones: the row wins the tie; the column (127 ones left)
+      beats the rows' single entries; then the residual is zero, every score ties at 0
+      and id 0 wins twice (a zero line);
+    - columns 20 and 10 all ones: the smaller column wins the tie, then the other;
+      then zero lines at id 0."""
+    cases = []
+    S = np.full((1, 128, 128), 0.5, np.float32)
+    cases.append((S, [0, 1, 2, 3]))
+    S = np.zeros((1, 128, 128), np.float32)
+    S[0, 5, :] = 1.0
+    S[0, :, 9] = 1.0
+    cases.append((S, [5, 128 + 9, 0, 0]))
+    S = np.zeros((1, 128, 128), np.float32)
+    S[0, :, 20] = 1.0
+    S[0, :, 10] = 1.0
+    cases.append((S, [128 + 10, 128 + 20, 0, 0]))
+    return cases

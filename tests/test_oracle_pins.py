@@ -19,7 +19,7 @@ import pytest
 import oracle
 from oracle import FoldDiag, OracleState
 from quantized_linear_attention_gb300 import workload as wlm
-from tests._helpers import code_mismatches, near_tie, rel_l2, tie_rows
+from tests._helpers import code_mismatches, near_tie, rel_l2, selection_ties, tie_rows
 
 
 # ---------------------------------------------------------------- dot products
@@ -439,3 +439,16 @@ def test_f5_rounds_exact_ties_to_even(bits):
     assert np.array_equal(dg[0].s_round[:3, :13] * 2, np.rint(dg[0].s_round[:3, :13] * 2))
     assert np.array_equal(st.codes, want)
     assert np.array_equal(st.sigma[0, :3], (np.float32(qm) * np.float32([0.5, 1.0, 2.0])) / np.float32(qm))
+
+
+# ---------------------------------------------------------------- F2 at exact score ties
+@pytest.mark.parametrize("case", range(3))
+def test_f2_exact_score_ties_go_to_the_smallest_id(case):
+    """Reading R5: among equal squared lengths the smallest id wins, so rows come before
+    columns and a smaller column before a larger one; once the residual is zero every score
+    ties at 0. Ties to the largest id, columns first or a one-shot top-C all miss one of
+    these hand-worked id lists."""
+    S0, want = selection_ties()[case]
+    st = OracleState(1, W=16, C=4)
+    st.init(S0)
+    assert st.comp_id[0, :4].tolist() == want

@@ -84,3 +84,27 @@ def test_exact_ties_round_to_even(bits):
     g.fold()
     assert np.array_equal(g.boundary()["codes"], want)
     assert g.status()[0] == lq.OK
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_selection_exact_score_ties(case):
+    """The init-fold and a later fold on states whose compensator selection meets exact
+    score ties: the hand-worked ids of the oracle's pin, and the whole boundary bit-exact."""
+    from oracle import FoldDiag, OracleState
+    from tests._gpu import GpuState, compare_boundary
+    from tests._helpers import selection_ties
+
+    S0, want = selection_ties()[case]
+    g = GpuState(1)
+    g.init(S0)
+    ref = OracleState(1, W=16, C=4)
+    dg = [FoldDiag(128, 128)]
+    ref.init(S0, diags=dg)
+    b = g.boundary()
+    assert b["comp_id"][0, :4].tolist() == want
+    compare_boundary(b, ref, [0], dg, what="init")
+    g.fold()
+    dg = [FoldDiag(128, 128)]
+    ref.fold(diags=dg)
+    compare_boundary(g.boundary(), ref, [0], dg, what="fold")
+    assert g.status()[0] == lq.OK
