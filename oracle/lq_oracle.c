@@ -3,9 +3,10 @@
  * per-window quantization with Compensator Tokens and residual smoothing).
  *
  * TEST INFRASTRUCTURE, NOT THE PRODUCT. Only the test suite, the smoke check
- * and the benchmark's CPU-baseline leg may load this library. It shares no code
- * with the CUDA path: no headers, helpers, tables or constants. It is written
- * as plain loops, one step at a time, in the order the method states them.
+ * and the benchmark's CPU-baseline leg and reference arm may load this library.
+ * It shares no code with the CUDA path: no headers, helpers, tables or
+ * constants. It is written as plain loops, one step at a time, in the order
+ * the method states them.
  *
  * Sources (pages; notation: state S is d_v x d_k, row i = value channel,
  * column j = key channel):

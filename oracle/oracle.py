@@ -1,7 +1,7 @@
 """Python front of the CPU oracle (``lq_oracle.c``).
 
 TEST INFRASTRUCTURE, NOT THE PRODUCT: only the test suite, ``__graft_entry__.smoke()``
-and the benchmark's CPU-baseline leg may import this module. It loads the oracle's
+and the benchmark's CPU-baseline leg and reference arm may import this module. It loads the oracle's
 own C library (built from ``oracle/lq_oracle.c`` by ``oracle/build.py``) and holds
 per-state arrays in numpy. No code here is shared with the CUDA path.
 
